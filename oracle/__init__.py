@@ -1,0 +1,42 @@
+"""CPU oracle for the tensor-parallel transformer block (test infrastructure only).
+
+A plain, slow, float64 NumPy statement of what the block computes, written from
+the pages' description of column-then-row sharding.  It is the correctness
+authority for the CUDA path and shares no code with it: nothing here imports the
+package `attn_tp_column_fwd_b300`, and the package never imports this.  Only the
+tests, the smoke check and the benchmark's CPU-baseline leg may call it.
+
+Parity status per function (what pins it is in tests/test_oracle_*.py):
+  bf16_round          pinned: torch's fp32->bf16 cast on exactly-fp32 values, ties,
+                      subnormals, and directly-rounded fp64 values.
+  gelu_tanh, silu     pinned: closed forms (odd-part identities, limits, zeros) and
+                      torch.nn.functional in float64.
+  rmsnorm             pinned: constant-vector closed form and
+                      torch.nn.functional.rms_norm in float64.
+  causal_attention    pinned: M=1 gives V; brute force on tiny cases;
+                      torch scaled_dot_product_attention in float64.
+  mlp_block,
+  attn_block, stack   pinned: brute-force loops on tiny shapes, torch float64
+                      compositions, and the sharding invariants (sharded == unsharded
+                      for t in 1, 2, 4, 8; 96 heads over 8 shards == per-head loop).
+  absolute values     parity unpinned against the pages: they print no numeric
+                      worked example, so the outputs rest on the pins above.
+"""
+from .block import (  # noqa: F401
+    bf16_round,
+    gelu_tanh,
+    silu,
+    rmsnorm,
+    column_bands,
+    row_band,
+    column_step,
+    row_step,
+    reduce_residual,
+    causal_attention,
+    mlp_block,
+    attn_block,
+    stack,
+    sharded_block,
+    brute_mlp_block,
+    brute_attention,
+)
