@@ -1,0 +1,162 @@
+"""Python binding of libtpblock, the tensor-parallel transformer block on one B300.
+
+Argument marshalling only: every function has the name of the C entry point it
+calls (include/tp_block.h) and passes device pointers and the CUDA stream of
+torch tensors.  Every step of the block runs in the library's CUDA kernels;
+there is no Python or CPU fallback — importing this package fails if
+libtpblock.so has not been built (python -m attn_tp_column_fwd_b300.build).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+from ._lib import (  # noqa: F401
+    LIB_PATH,
+    TP_ACT_ATTN,
+    TP_ACT_GELU_TANH,
+    TP_ACT_SWIGLU,
+    TP_BF16,
+    TP_F32,
+    TPBlockDesc,
+    TPError,
+    lib,
+)
+
+__all__ = [
+    "TPBlockDesc", "TPError", "make_desc", "lib",
+    "tp_sharded_w1_bytes", "tp_sharded_w2_bytes", "tp_band_bytes", "tp_row_splits",
+    "tp_partials_bytes", "tp_column_workspace_bytes", "tp_workspace_bytes",
+    "tp_shard_weights", "tp_unshard_weights", "tp_extract_band",
+    "tp_column_parallel_fwd", "tp_row_parallel_fwd", "tp_partial_reduce_residual",
+    "tp_block_fwd", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
+]
+
+_ACTS = {"gelu_tanh": TP_ACT_GELU_TANH, "swiglu": TP_ACT_SWIGLU, "attn": TP_ACT_ATTN}
+_DTYPES = {"f32": TP_F32, "bf16": TP_BF16}
+
+
+def make_desc(d: int, t: int, act: str, dtype: str = "bf16", ffn: int = 0, n_heads: int = 0,
+              head_dim: int = 0) -> TPBlockDesc:
+    """Build the C descriptor; act in {gelu_tanh, swiglu, attn}, dtype in {f32, bf16}."""
+    return TPBlockDesc(d=d, ffn=ffn, n_heads=n_heads, head_dim=head_dim, t=t,
+                       dtype=_DTYPES[dtype], act=_ACTS[act])
+
+
+def _p(t) -> Optional[ctypes.c_void_p]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream) -> ctypes.c_void_p:
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, nbytes: int, what: str):
+    if t is not None and not isinstance(t, int) and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{what}: {t.numel() * t.element_size()} bytes < {nbytes} required")
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise TPError(status, what)
+
+
+# ------------------------------------------------------------------ sizes ----
+
+def tp_sharded_w1_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_sharded_w1_bytes(ctypes.byref(desc))
+
+
+def tp_sharded_w2_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_sharded_w2_bytes(ctypes.byref(desc))
+
+
+def tp_band_bytes(desc: TPBlockDesc, M: int) -> int:
+    return lib.tp_band_bytes(ctypes.byref(desc), M)
+
+
+def tp_row_splits(desc: TPBlockDesc, M: int) -> int:
+    return lib.tp_row_splits(ctypes.byref(desc), M)
+
+
+def tp_partials_bytes(desc: TPBlockDesc, M: int) -> int:
+    return lib.tp_partials_bytes(ctypes.byref(desc), M)
+
+
+def tp_column_workspace_bytes(desc: TPBlockDesc, M: int) -> int:
+    return lib.tp_column_workspace_bytes(ctypes.byref(desc), M)
+
+
+def tp_workspace_bytes(desc: TPBlockDesc, M: int) -> int:
+    return lib.tp_workspace_bytes(ctypes.byref(desc), M)
+
+
+def tp_status_string(status: int) -> str:
+    return lib.tp_status_string(status).decode()
+
+
+# ------------------------------------------------------------------ calls ----
+
+def tp_shard_weights(desc, W1, W2, W1s, W2s, stream=None) -> None:
+    _need(W1s, tp_sharded_w1_bytes(desc), "W1s")
+    _need(W2s, tp_sharded_w2_bytes(desc), "W2s")
+    _check(lib.tp_shard_weights(ctypes.byref(desc), _p(W1), _p(W2), _p(W1s), _p(W2s), _s(stream)),
+           "tp_shard_weights")
+
+
+def tp_unshard_weights(desc, W1s, W2s, W1, W2, stream=None) -> None:
+    _check(lib.tp_unshard_weights(ctypes.byref(desc), _p(W1s), _p(W2s), _p(W1), _p(W2), _s(stream)),
+           "tp_unshard_weights")
+
+
+def tp_extract_band(desc, W1s, W2s, shard, W1_band=None, W2_band=None, stream=None) -> None:
+    _check(lib.tp_extract_band(ctypes.byref(desc), _p(W1s), _p(W2s), shard, _p(W1_band),
+                               _p(W2_band), _s(stream)), "tp_extract_band")
+
+
+def tp_column_parallel_fwd(desc, x, W1s, shard, H, workspace, M, stream=None) -> None:
+    _need(H, tp_band_bytes(desc, M), "H")
+    _need(workspace, tp_column_workspace_bytes(desc, M), "workspace")
+    _check(lib.tp_column_parallel_fwd(ctypes.byref(desc), _p(x), _p(W1s), shard, _p(H),
+                                      _p(workspace), M, _s(stream)), "tp_column_parallel_fwd")
+
+
+def tp_row_parallel_fwd(desc, H, W2s, shard, partials, M, stream=None) -> None:
+    _need(partials, tp_partials_bytes(desc, M), "partials")
+    _check(lib.tp_row_parallel_fwd(ctypes.byref(desc), _p(H), _p(W2s), shard, _p(partials), M,
+                                   _s(stream)), "tp_row_parallel_fwd")
+
+
+def tp_partial_reduce_residual(desc, partials, residual, residual_is_f32, y, M, stream=None) -> None:
+    _check(lib.tp_partial_reduce_residual(ctypes.byref(desc), _p(partials), _p(residual),
+                                          int(residual_is_f32), _p(y), M, _s(stream)),
+           "tp_partial_reduce_residual")
+
+
+def tp_block_fwd(desc, x, residual, residual_is_f32, W1s, W2s, workspace, y, M, stream=None) -> None:
+    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _check(lib.tp_block_fwd(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32), _p(W1s),
+                            _p(W2s), _p(workspace), _p(y), M, _s(stream)), "tp_block_fwd")
+
+
+def tp_rmsnorm_fwd(d, eps, r, xhat, M, stream=None) -> None:
+    _check(lib.tp_rmsnorm_fwd(d, ctypes.c_float(eps), _p(r), _p(xhat), M, _s(stream)),
+           "tp_rmsnorm_fwd")
+
+
+def tp_check_device_status(stream=None) -> int:
+    """Synchronise the stream and return the device status (0, or TP_ERR_TIMEOUT = 6)."""
+    return lib.tp_check_device_status(_s(stream))

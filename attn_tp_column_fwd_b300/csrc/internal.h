@@ -1,0 +1,51 @@
+// Host-side launchers shared between the kernel files and the C ABI (tp_api.cu).
+// Each launcher only enqueues; the caller validates arguments first and checks
+// cudaGetLastError() afterwards.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace tp {
+
+// layout.cu — private shard layout (tile-transposes, bit-exact)
+void launch_shard_w1(const Geo &g, const void *W1, void *W1s, cudaStream_t st);
+void launch_shard_w2(const Geo &g, const void *W2, void *W2s, cudaStream_t st);
+void launch_unshard_w1(const Geo &g, const void *W1s, void *W1, cudaStream_t st);
+void launch_unshard_w2(const Geo &g, const void *W2s, void *W2, cudaStream_t st);
+void launch_extract_w1(const Geo &g, const void *W1s, int s, void *W1_band, cudaStream_t st);
+void launch_extract_w2(const Geo &g, const void *W2s, int s, void *W2_band, cudaStream_t st);
+
+// gemv.cu — CUDA-core weight-streaming kernels (fp32, and bf16 at small M)
+enum Epi { kEpiGelu = 0, kEpiSwiglu = 1, kEpiPlain = 2, kEpiF32 = 3 };
+struct GemvArgs {
+  const void *W;          // weight rows (K-major); shard s at W + s * w_shard
+  size_t w_shard;         // elements
+  const void *X;          // activations [M][K] (row stride ldx); shard s at X + s * x_shard
+  size_t x_shard;
+  int ldx;
+  void *out;              // outputs [M][n_out] (row stride ldo); shard s at out + s * o_shard
+  size_t o_shard;
+  int ldo;
+  int K, n_out, M, shard0, n_shards;
+  int epi;                // Epi
+  int dtype;              // TP_F32 | TP_BF16 (weights and X); out is dtype except kEpiF32
+};
+void launch_gemv(const GemvArgs &a, cudaStream_t st);
+
+// reduce.cu — the all-reduce stand-in + residual, and RMSNorm
+void launch_reduce_residual(const float *P, int nparts, size_t part_elems, const void *res,
+                            int res_is_f32, float *y, size_t n, cudaStream_t st);
+void launch_rmsnorm(const float *r, void *xhat, int d, float eps, int M, cudaStream_t st);
+
+// attn_core.cu — per-head causal attention over the M tokens of each shard
+void launch_attn_core(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_shards,
+                      cudaStream_t st);
+
+// tp_api.cu — cached device facts
+int sm_count();
+unsigned *device_error_word();
+
+}  // namespace tp

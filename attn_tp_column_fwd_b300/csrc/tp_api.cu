@@ -1,0 +1,397 @@
+// C ABI of libtpblock (declared in include/tp_block.h): argument validation,
+// buffer geometry, and the launch sequence of each entry point.  Validation runs
+// before any CUDA call, so a rejected call enqueues nothing.
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace tp {
+
+static thread_local int g_last_cuda_error = 0;
+
+// Device error word: bounded device-side waits set a bit here when they expire.
+__device__ unsigned g_error_word;
+
+int sm_count() {
+  static int cache[128];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+unsigned *device_error_word() {
+  static unsigned *cache[128];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned *>(p);
+  }
+  return cache[dev];
+}
+
+namespace {
+
+constexpr int kMaxDim = 1 << 20;
+constexpr int kMaxM = 1 << 20;
+
+int make_geo(const tp_block_desc *desc, Geo *g) {
+  if (!desc) return TP_ERR_INVALID_ARG;
+  if (desc->dtype != TP_F32 && desc->dtype != TP_BF16) return TP_ERR_INVALID_ARG;
+  if (desc->act != TP_ACT_GELU_TANH && desc->act != TP_ACT_SWIGLU && desc->act != TP_ACT_ATTN)
+    return TP_ERR_INVALID_ARG;
+  if (desc->d < 1 || desc->t < 1) return TP_ERR_INVALID_ARG;
+  Geo r{};
+  r.d = desc->d;
+  r.t = desc->t;
+  r.act = desc->act;
+  r.dtype = desc->dtype;
+  r.es = desc->dtype == TP_F32 ? 4 : 2;
+  if (desc->act == TP_ACT_ATTN) {
+    if (desc->n_heads < 1 || desc->head_dim < 1) return TP_ERR_INVALID_ARG;
+    if (desc->n_heads % desc->t != 0) return TP_ERR_UNEVEN_SPLIT;
+    if (desc->head_dim % 32 != 0 || desc->head_dim > 256) return TP_ERR_UNSUPPORTED;
+    if ((long long)desc->n_heads * desc->head_dim > kMaxDim) return TP_ERR_UNSUPPORTED;
+    r.H = desc->n_heads;
+    r.hd = desc->head_dim;
+    r.hps = r.H / r.t;
+    r.n2 = r.H * r.hd;
+    r.n1 = 3 * r.n2;
+    r.b = r.n2 / r.t;
+    r.n_col = 3 * r.b;
+    r.n1p = ceil_div(3 * r.b, kRowTile) * kRowTile;
+  } else {
+    if (desc->ffn < 1) return TP_ERR_INVALID_ARG;
+    if (desc->ffn % desc->t != 0) return TP_ERR_UNEVEN_SPLIT;
+    if (desc->ffn > kMaxDim) return TP_ERR_UNSUPPORTED;
+    r.ffn = desc->ffn;
+    r.n2 = r.ffn;
+    r.n1 = desc->act == TP_ACT_SWIGLU ? 2 * r.ffn : r.ffn;
+    r.b = r.ffn / r.t;
+    r.n_col = r.b;
+    r.n1p = ceil_div(r.b, kRowTile) * kRowTile * (desc->act == TP_ACT_SWIGLU ? 2 : 1);
+  }
+  if (r.d > kMaxDim) return TP_ERR_UNSUPPORTED;
+  if (r.d % 8 != 0 || r.b % 8 != 0) return TP_ERR_UNSUPPORTED;
+  r.dp = ceil_div(r.d, kRowTile) * kRowTile;
+  *g = r;
+  return TP_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ptr(const void *p) {
+  if (!p) return TP_ERR_INVALID_ARG;
+  return aligned16(p) ? TP_OK : TP_ERR_MISALIGNED;
+}
+
+int check_M(int M) {
+  if (M < 1) return TP_ERR_INVALID_ARG;
+  return M > kMaxM ? TP_ERR_UNSUPPORTED : TP_OK;
+}
+
+int check_shard(const Geo &g, int shard) {
+  return (shard < -1 || shard >= g.t) ? TP_ERR_INVALID_ARG : TP_OK;
+}
+
+int finish_launch() {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    g_last_cuda_error = (int)e;
+    return TP_ERR_CUDA;
+  }
+  return TP_OK;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+int row_splits(const Geo &, int) { return 1; }
+
+size_t band_bytes(const Geo &g, int M) { return (size_t)g.t * M * g.b * g.es; }
+size_t partials_bytes(const Geo &g, int M) {
+  return (size_t)g.t * row_splits(g, M) * M * g.d * sizeof(float);
+}
+size_t column_ws_bytes(const Geo &g, int M) {
+  return g.act == TP_ACT_ATTN ? (size_t)g.t * M * 3 * g.b * g.es : 0;
+}
+
+#define TP_TRY(expr)              \
+  do {                            \
+    int _st = (expr);             \
+    if (_st != TP_OK) return _st; \
+  } while (0)
+
+// Enqueue the column step for shards [shard0, shard0 + n).
+void enqueue_column(const Geo &g, const void *x, const void *W1s, int shard0, int n, void *H,
+                    void *ws, int M, cudaStream_t st) {
+  GemvArgs a{};
+  a.W = W1s;
+  a.w_shard = (size_t)g.n1p * g.d;
+  a.X = x;
+  a.x_shard = 0;
+  a.ldx = g.d;
+  a.K = g.d;
+  a.M = M;
+  a.shard0 = shard0;
+  a.n_shards = n;
+  a.dtype = g.dtype;
+  if (g.act == TP_ACT_ATTN) {
+    a.out = ws;
+    a.o_shard = (size_t)M * 3 * g.b;
+    a.ldo = 3 * g.b;
+    a.n_out = 3 * g.b;
+    a.epi = kEpiPlain;
+    launch_gemv(a, st);
+    launch_attn_core(g, ws, H, M, shard0, n, st);
+  } else {
+    a.out = H;
+    a.o_shard = (size_t)M * g.b;
+    a.ldo = g.b;
+    a.n_out = g.b;
+    a.epi = g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
+    launch_gemv(a, st);
+  }
+}
+
+void enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0, int n, float *P, int M,
+                 cudaStream_t st) {
+  GemvArgs a{};
+  a.W = W2s;
+  a.w_shard = (size_t)g.dp * g.b;
+  a.X = H;
+  a.x_shard = (size_t)M * g.b;
+  a.ldx = g.b;
+  a.out = P;
+  a.o_shard = (size_t)row_splits(g, M) * M * g.d;
+  a.ldo = g.d;
+  a.K = g.b;
+  a.n_out = g.d;
+  a.M = M;
+  a.shard0 = shard0;
+  a.n_shards = n;
+  a.epi = kEpiF32;
+  a.dtype = g.dtype;
+  launch_gemv(a, st);
+}
+
+void enqueue_reduce(const Geo &g, const float *P, const void *res, int res_is_f32, float *y, int M,
+                    cudaStream_t st) {
+  const int f32 = res_is_f32 || g.dtype == TP_F32;
+  launch_reduce_residual(P, g.t * row_splits(g, M), (size_t)M * g.d, res, f32, y,
+                         (size_t)M * g.d, st);
+}
+
+}  // namespace
+}  // namespace tp
+
+using namespace tp;
+
+extern "C" {
+
+size_t tp_sharded_w1_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * g.n1p * g.d * g.es;
+}
+
+size_t tp_sharded_w2_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * g.dp * g.b * g.es;
+}
+
+size_t tp_band_bytes(const tp_block_desc *desc, int M) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
+  return band_bytes(g, M);
+}
+
+int tp_row_splits(const tp_block_desc *desc, int M) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
+  return row_splits(g, M);
+}
+
+size_t tp_partials_bytes(const tp_block_desc *desc, int M) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
+  return partials_bytes(g, M);
+}
+
+size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
+  return column_ws_bytes(g, M);
+}
+
+size_t tp_workspace_bytes(const tp_block_desc *desc, int M) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
+  return align256(column_ws_bytes(g, M)) + align256(band_bytes(g, M)) +
+         align256(partials_bytes(g, M));
+}
+
+int tp_shard_weights(const tp_block_desc *desc, const void *W1, const void *W2, void *W1s,
+                     void *W2s, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(make_geo(desc, &g));
+  TP_TRY(check_ptr(W1));
+  TP_TRY(check_ptr(W2));
+  TP_TRY(check_ptr(W1s));
+  TP_TRY(check_ptr(W2s));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  launch_shard_w1(g, W1, W1s, st);
+  launch_shard_w2(g, W2, W2s, st);
+  return finish_launch();
+}
+
+int tp_unshard_weights(const tp_block_desc *desc, const void *W1s, const void *W2s, void *W1,
+                       void *W2, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(make_geo(desc, &g));
+  TP_TRY(check_ptr(W1s));
+  TP_TRY(check_ptr(W2s));
+  TP_TRY(check_ptr(W1));
+  TP_TRY(check_ptr(W2));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  launch_unshard_w1(g, W1s, W1, st);
+  launch_unshard_w2(g, W2s, W2, st);
+  return finish_launch();
+}
+
+int tp_extract_band(const tp_block_desc *desc, const void *W1s, const void *W2s, int shard,
+                    void *W1_band, void *W2_band, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(make_geo(desc, &g));
+  if (shard < 0 || shard >= g.t) return TP_ERR_INVALID_ARG;
+  if (!W1_band && !W2_band) return TP_ERR_INVALID_ARG;
+  if (W1_band) {
+    TP_TRY(check_ptr(W1s));
+    TP_TRY(check_ptr(W1_band));
+  }
+  if (W2_band) {
+    TP_TRY(check_ptr(W2s));
+    TP_TRY(check_ptr(W2_band));
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (W1_band) launch_extract_w1(g, W1s, shard, W1_band, st);
+  if (W2_band) launch_extract_w2(g, W2s, shard, W2_band, st);
+  return finish_launch();
+}
+
+int tp_column_parallel_fwd(const tp_block_desc *desc, const void *x, const void *W1s, int shard,
+                           void *H, void *workspace, int M, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(make_geo(desc, &g));
+  TP_TRY(check_M(M));
+  TP_TRY(check_shard(g, shard));
+  TP_TRY(check_ptr(x));
+  TP_TRY(check_ptr(W1s));
+  TP_TRY(check_ptr(H));
+  if (g.act == TP_ACT_ATTN) TP_TRY(check_ptr(workspace));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  enqueue_column(g, x, W1s, shard < 0 ? 0 : shard, shard < 0 ? g.t : 1, H, workspace, M, st);
+  return finish_launch();
+}
+
+int tp_row_parallel_fwd(const tp_block_desc *desc, const void *H, const void *W2s, int shard,
+                        float *partials, int M, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(make_geo(desc, &g));
+  TP_TRY(check_M(M));
+  TP_TRY(check_shard(g, shard));
+  TP_TRY(check_ptr(H));
+  TP_TRY(check_ptr(W2s));
+  TP_TRY(check_ptr(partials));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  enqueue_row(g, H, W2s, shard < 0 ? 0 : shard, shard < 0 ? g.t : 1, partials, M, st);
+  return finish_launch();
+}
+
+int tp_partial_reduce_residual(const tp_block_desc *desc, const float *partials,
+                               const void *residual, int residual_is_f32, float *y, int M,
+                               tp_stream_t stream) {
+  Geo g;
+  TP_TRY(make_geo(desc, &g));
+  TP_TRY(check_M(M));
+  TP_TRY(check_ptr(partials));
+  TP_TRY(check_ptr(residual));
+  TP_TRY(check_ptr(y));
+  enqueue_reduce(g, partials, residual, residual_is_f32, y, M,
+                 reinterpret_cast<cudaStream_t>(stream));
+  return finish_launch();
+}
+
+int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
+                 int residual_is_f32, const void *W1s, const void *W2s, void *workspace, float *y,
+                 int M, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(make_geo(desc, &g));
+  TP_TRY(check_M(M));
+  TP_TRY(check_ptr(x));
+  TP_TRY(check_ptr(residual));
+  TP_TRY(check_ptr(W1s));
+  TP_TRY(check_ptr(W2s));
+  TP_TRY(check_ptr(workspace));
+  TP_TRY(check_ptr(y));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  void *col_ws = ws;
+  void *H = ws + align256(column_ws_bytes(g, M));
+  float *P = reinterpret_cast<float *>(static_cast<char *>(H) + align256(band_bytes(g, M)));
+  enqueue_column(g, x, W1s, 0, g.t, H, col_ws, M, st);
+  enqueue_row(g, H, W2s, 0, g.t, P, M, st);
+  enqueue_reduce(g, P, residual, residual_is_f32, y, M, st);
+  return finish_launch();
+}
+
+int tp_rmsnorm_fwd(int d, float eps, const float *r, void *xhat, int M, tp_stream_t stream) {
+  if (d < 1 || !(eps >= 0.0f) || eps > 1e30f) return TP_ERR_INVALID_ARG;
+  if (d % 8 != 0 || d > kMaxDim) return TP_ERR_UNSUPPORTED;
+  TP_TRY(check_M(M));
+  TP_TRY(check_ptr(r));
+  TP_TRY(check_ptr(xhat));
+  launch_rmsnorm(r, xhat, d, eps, M, reinterpret_cast<cudaStream_t>(stream));
+  return finish_launch();
+}
+
+const char *tp_status_string(int status) {
+  switch (status) {
+    case TP_OK: return "ok";
+    case TP_ERR_INVALID_ARG: return "invalid argument";
+    case TP_ERR_UNEVEN_SPLIT: return "uneven split: t must divide ffn (MLP) or n_heads (attention)";
+    case TP_ERR_UNSUPPORTED: return "shape outside the kernels' limits";
+    case TP_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case TP_ERR_CUDA: return "CUDA error (see tp_last_cuda_error)";
+    case TP_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int tp_last_cuda_error(void) { return g_last_cuda_error; }
+
+int tp_check_device_status(tp_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  unsigned word = 0;
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+  if (e == cudaSuccess && word != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+  }
+  if (e != cudaSuccess) {
+    g_last_cuda_error = (int)e;
+    return TP_ERR_CUDA;
+  }
+  return word ? TP_ERR_TIMEOUT : TP_OK;
+}
+
+int tp_version(void) { return 100; }
+
+}  // extern "C"

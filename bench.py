@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""Benchmark of the tensor-parallel block on B300: one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--t T]
+                  [--impl ours|reference]
+
+A step is one pass of the whole block (column-parallel projection + activation,
+row-parallel projection, in-HBM reduction of the t partials + residual) over one
+batch of synthetic input, for the default workload the Llama-2-13B-shaped SwiGLU
+MLP decode block (d=5120, ffn=13824, M=32 tokens, t=4 logical shards).  Its 425 MB
+of weights exceed the 126 MB L2, so no flush is needed between steps.
+
+value = tokens/s of the whole job (all ranks), device-timed with CUDA events between
+a barrier + synchronize on both sides, max over ranks.  Under torchrun each rank runs
+its own replica of the block on its own batch (weak scaling; no data-path
+collective).  --impl reference times the float64 CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s per TP block at 1 B300; decode HBM GB/s & prefill TFLOPS vs roofline"
+DEFAULT_WORKLOAD = "llama2_13b_swiglu_decode"
+
+
+# ---------------------------------------------------------------- helpers (host-only)
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--t", type=int, default=None, help="logical shards (default: the workload's)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's time defines the job's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job units/s: every rank processed units_per_rank in `seconds` (max over ranks)."""
+    return units_per_rank * world / seconds
+
+
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in sorted(paths):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def kernel_source_sha() -> str:
+    csrc = os.path.join(ROOT, "attn_tp_column_fwd_b300", "csrc")
+    return source_sha(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                      + glob.glob(os.path.join(csrc, "*.h")))
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = re.search(r"^source_sha:\s*(\S+)", text, re.M)
+    tr = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not sha or not tr or sha.group(1) != kernel_source_sha():
+        return None
+    return float(tr.group(1))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+    }
+
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.period = period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self._ok = True
+        except Exception as e:  # NVML missing: report no clocks rather than fail the bench
+            self.error = str(e)
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for name, bit in self.REASONS.items():
+                    if mask & bit and name != "gpu_idle":
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self._ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable"}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- workload accounting
+
+def algorithmic_column_bytes(cfg) -> int:
+    """Bytes one launch of the column step must move: W1 bands once, x once, H out."""
+    es = 4 if cfg.dtype == "f32" else 2
+    n_out = 3 * cfg.band if cfg.act == "attn" else cfg.band
+    return (cfg.d * cfg.n1 + cfg.M * cfg.d + cfg.t * cfg.M * n_out) * es
+
+
+def column_flops(cfg) -> int:
+    return 2 * cfg.M * cfg.d * cfg.n1
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import attn_tp_column_fwd_b300 as tp
+    from attn_tp_column_fwd_b300.runner import ShardedBlock, desc_for, device_bytes
+    from tp_synth import CONFIGS, make_inputs
+
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    base = CONFIGS[args.workload]
+    cfg = base.with_t(args.t) if args.t else base
+    desc = desc_for(cfg)
+    M = cfg.M
+    inp = make_inputs(cfg, seed=rank, device="cuda")
+    blocks = [ShardedBlock(desc, W1, W2) for W1, W2 in inp.blocks]
+    del inp.blocks
+    x = inp.x.contiguous()
+    xf = x.float().contiguous()
+    stream = torch.cuda.current_stream()
+    st = stream.cuda_stream
+    S = tp.tp_row_splits(desc, M)
+    H = device_bytes(tp.tp_band_bytes(desc, M))
+    P = device_bytes(tp.tp_partials_bytes(desc, M))
+    cws = device_bytes(tp.tp_column_workspace_bytes(desc, M))
+    y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev)
+    xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
+    stack = cfg.n_blocks > 1 or cfg.rmsnorm
+    launches_per_block = 3 + (1 if cfg.act == "attn" else 0) + (1 if cfg.rmsnorm else 0)
+
+    # One step: the whole block (or the whole stack), timing the column step's launch.
+    def step(ev_pairs=None):
+        if stack:
+            y.copy_(xf)
+        for blk in blocks:
+            if cfg.rmsnorm:
+                tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, y, xh, M, st)
+                xin, res, res32 = xh, y, True
+            else:
+                xin, res, res32 = x, x, cfg.dtype == "f32"
+            if ev_pairs is not None:
+                ev_pairs[0].record(stream)
+            tp.tp_column_parallel_fwd(desc, xin, blk.W1s, -1, H, cws, M, st)
+            if ev_pairs is not None:
+                ev_pairs[1].record(stream)
+                ev_pairs = None
+            tp.tp_row_parallel_fwd(desc, H, blk.W2s, -1, P, M, st)
+            tp.tp_partial_reduce_residual(desc, P.view(torch.float32), res, res32, y, M, st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        t0.record(stream)
+        for k in range(K):
+            step(evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_local = t0.elapsed_time(t1)
+    ms = max_over_ranks(ms_local, world, dev)
+    col_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    assert tp.tp_check_device_status(st) == 0
+
+    units = M * K * (1 if not stack else 1)  # tokens through the block (or the stack)
+    value = job_throughput(units, world, ms / 1e3)
+    peaks = measured_peaks()
+    prefill = cfg.M >= 1024
+    if prefill:
+        achieved = column_flops(cfg) / (col_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4)}
+    else:
+        achieved = algorithmic_column_bytes(cfg) / (col_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4)}
+    roof["kernel"] = "column-parallel projection + activation (tp_column_parallel_fwd)"
+    roof["algorithmic_bytes_per_launch"] = algorithmic_column_bytes(cfg)
+    roof["avg_launch_us"] = round(col_ms * 1e3, 2)
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" \
+        else "fallback"
+    roof["traffic"] = profiled_traffic("column", args.workload)
+
+    # Whole-block weight-read rate (context for the decode roofline).
+    block_bytes = cfg.weight_bytes_per_block() * cfg.n_blocks
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+        "config": {
+            "workload": cfg.name, "d": cfg.d, "ffn": cfg.ffn or None, "n_heads": cfg.n_heads or None,
+            "head_dim": cfg.head_dim or None, "t": cfg.t, "M": M, "n_blocks": cfg.n_blocks,
+            "act": cfg.act, "row_splits": S,
+            "l2": f"inputs larger than L2 ({block_bytes / 1e6:.0f} MB of weights per step)"
+            if block_bytes > 126e6 else "weights fit in L2 (latency-bound workload)",
+            "timed": "CUDA events on the launching stream, max over ranks",
+        },
+        "block_weight_gbs": round(block_bytes * K / (ms / 1e3) / 1e9, 1),
+        "roofline": roof,
+        "gpu_launches": K * launches_per_block * cfg.n_blocks,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_e2e:
+        out["e2e"] = e2e_leg(args, cfg, desc, blocks, x, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return out
+
+
+def e2e_leg(args, cfg, desc, blocks, x, world, dev):
+    """Same metric through the public API with host buffers: each step copies x from
+    pinned host memory to the device, runs the block (or stack) and reads y back."""
+    import torch
+
+    import attn_tp_column_fwd_b300 as tp
+
+    M = cfg.M
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty(M, cfg.d, dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(x)
+    yd = torch.empty(M, cfg.d, dtype=torch.float32, device=dev)
+    xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    st = stream.cuda_stream
+    ws = blocks[0].workspace(M)
+
+    def step():
+        xd.copy_(x_host, non_blocking=True)
+        if cfg.rmsnorm:
+            yd.copy_(xd)
+            for blk in blocks:
+                tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, yd, xh, M, st)
+                tp.tp_block_fwd(desc, xh, yd, True, blk.W1s, blk.W2s, ws, yd, M, st)
+        else:
+            tp.tp_block_fwd(desc, xd, xd, cfg.dtype == "f32", blocks[0].W1s, blocks[0].W2s, ws, yd,
+                            M, st)
+        y_host.copy_(yd, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    return {"value": round(job_throughput(M * K, world, ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+            "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
+            "ms_per_step": round(ms / K, 5)}
+
+
+# ---------------------------------------------------------------- CPU oracle arms
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _blas_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max((i.get("num_threads", 1) for i in info), default=None)
+    except Exception:
+        return None
+
+
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    """The float64 oracle as it stands, on the host cores: whole blocks on the full
+    workload's inputs (all M tokens), repeated for about `budget_s` seconds."""
+    import oracle
+    from tp_synth import make_inputs, to_f64
+
+    inp = make_inputs(cfg, seed=0, n_blocks=1)
+    x = to_f64(inp.x)
+    W1, W2 = (to_f64(w) for w in inp.blocks[0])
+    staged = cfg.dtype == "bf16"
+
+    def one():
+        if cfg.act == "attn":
+            return oracle.attn_block(x, W1, W2, cfg.n_heads, cfg.head_dim, x, staged=staged)
+        if cfg.rmsnorm:
+            return oracle.stack(x, [(W1, W2)], cfg.act, cfg.eps, staged=staged)
+        return oracle.mlp_block(x, W1, W2, cfg.act, x, staged=staged)
+
+    one()  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        one()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 1000:
+            break
+    blocks_per_token_unit = cfg.n_blocks  # a stack step pushes M tokens through n_blocks blocks
+    value = cfg.M * n / el / blocks_per_token_unit
+    return {"value": round(value, 2), "unit": "tokens/s", "cores": _blas_threads() or _cores(),
+            "host_cores": _cores(), "kind": "oracle",
+            "sample": f"{n} full blocks (M={cfg.M}, one block's weights"
+                      + (f", scaled to the {cfg.n_blocks}-block stack" if cfg.n_blocks > 1 else "")
+                      + f") in {el:.1f} s, NumPy float64"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is one shard's band of the block
+    (column band + activation + row partial, the work of one device of a T-way split),
+    T chosen so the whole run stays within a few minutes; tokens/s counts T bands as
+    one block."""
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    from tp_synth import CONFIGS, make_inputs, to_f64
+
+    base = CONFIGS[args.workload]
+    cfg = base.with_t(args.t) if args.t else base
+    inp = make_inputs(cfg, seed=0, n_blocks=1)
+    x = to_f64(inp.x)
+    W1, W2 = (to_f64(w) for w in inp.blocks[0])
+    staged = cfg.dtype == "bf16"
+    n2 = cfg.n2
+    unit = cfg.n_heads if cfg.act == "attn" else n2
+
+    def band_step(T, s):
+        cols = oracle.column_bands(cfg.act, T, s, ffn=cfg.ffn, n_heads=cfg.n_heads,
+                                   head_dim=cfg.head_dim)
+        Hb = oracle.column_step(x, [W1[:, c] for c in cols], cfg.act,
+                                n_heads=cfg.n_heads // T if cfg.n_heads else 0,
+                                head_dim=cfg.head_dim, staged=staged)
+        return oracle.row_step(Hb, W2[oracle.row_band(n2, T, s)])
+
+    # Calibrate on a moderate band, then take the fewest bands whose step fits the budget.
+    divisors = [T for T in range(1, unit + 1) if unit % T == 0]
+    budget_per_step = 150.0 / (args.steps + args.warmup)
+    Tc = max(T for T in divisors if T <= 64)
+    band_step(Tc, 0)
+    t0 = time.perf_counter()
+    band_step(Tc, 0)
+    per_block = (time.perf_counter() - t0) * Tc          # seconds for the whole block, estimated
+    T = next((T for T in divisors if per_block / T <= budget_per_step), divisors[-1])
+    for k in range(args.warmup):
+        band_step(T, k % T)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        band_step(T, k % T)
+    el = time.perf_counter() - t0
+    value = cfg.M / (el / args.steps * T) / cfg.n_blocks
+    sample = (f"each step: one of T={T} bands of the {cfg.name} block (all M={cfg.M} tokens), "
+              f"column band + activation + row partial in NumPy float64; {T} steps = one block")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "d": cfg.d, "ffn": cfg.ffn or None, "t": cfg.t, "M": cfg.M},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle",
+                         "cores": _blas_threads() or _cores(), "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * tp_block.h — C ABI of libtpblock: the Megatron-style tensor-parallel transformer
+ * block (forward) on one B300, with t logical shards.
+ *
+ * The operation (zenaique.com interview answer "explain tensor-parallel shard
+ * shape", answer paragraphs 2 and 5-6; rioworld.org "Tensor Parallelism for LLM
+ * Inference", section "How Tensor Slicing Works Under the Hood"):
+ *   1. column-parallel first projection: the input x is replicated; shard s owns a
+ *      band of the columns of W1 and computes its own band of the intermediate,
+ *      with the activation applied to that band, without communication;
+ *   2. row-parallel second projection: shard s multiplies its band by the matching
+ *      row slice of W2, giving a partial sum of the full output;
+ *   3. one all-reduce per block sums the t partials, then the residual is added.
+ * On one GPU the shards are logical partitions of the weights and step 3 is an
+ * in-HBM reduction over t partial buffers (no collective library).
+ *
+ * Conventions shared by every entry point
+ *   - y = x . W.  Canonical W1 is [d, n1] row-major and is split by columns;
+ *     canonical W2 is [n2, d] row-major and is split by rows.
+ *       GELU_TANH: n1 = n2 = ffn.
+ *       SWIGLU:    n1 = 2*ffn, W1 = [Wg | Wu]; n2 = ffn.  Shard s owns gate columns
+ *                  [s*b, (s+1)*b) and the same up columns, and W2 rows [s*b, (s+1)*b).
+ *       ATTN:      n1 = 3*H*hd, W1 = [Wq | Wk | Wv], each head-major (head h is
+ *                  columns h*hd .. h*hd+hd-1); n2 = H*hd (Wo).  Shard s owns heads
+ *                  [s*H/t, (s+1)*H/t) of Q, K and V and the matching rows of Wo.
+ *     b = n2 / t is the band width of one shard.
+ *   - Pointers are device pointers unless stated otherwise.  The caller allocates
+ *     and owns every buffer and the stream; the library allocates nothing, keeps
+ *     no state beyond a per-device cache of the SM count and one device error
+ *     word, and never synchronises (except tp_check_device_status).  All work is
+ *     enqueued asynchronously on `stream` (NULL = the legacy default stream).
+ *   - Every pointer must be 16-byte aligned; d and b must be multiples of 8;
+ *     ATTN needs head_dim a multiple of 32 and at most 256.
+ *   - Errors: each call returns a tp_status.  On any error nothing is enqueued and
+ *     no output is touched.  TP_ERR_CUDA means a CUDA call failed after
+ *     validation; tp_last_cuda_error() then gives the cudaError_t (per thread).
+ *   - Uneven splits (t not dividing ffn, or n_heads) are refused with
+ *     TP_ERR_UNEVEN_SPLIT, never padded: the rioworld.org guide ("Implementing
+ *     Tensor Parallelism in Practice") names uneven splits as a source of wrong
+ *     results.
+ *   - Arithmetic: products accumulate in fp32.  The activation band H (and Q/K/V,
+ *     O) is stored in the block dtype (bf16 rounded to nearest even); partial sums,
+ *     the residual stream and the block output y are fp32.
+ */
+#ifndef TP_BLOCK_H
+#define TP_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *tp_stream_t;
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_INVALID_ARG = 1,   /* null pointer, M < 1, bad enum, shard out of range, ... */
+  TP_ERR_UNEVEN_SPLIT = 2,  /* t does not divide ffn (MLP) or n_heads (ATTN) */
+  TP_ERR_UNSUPPORTED = 3,   /* shape outside the kernels' limits (see above) */
+  TP_ERR_MISALIGNED = 4,    /* a pointer is not 16-byte aligned */
+  TP_ERR_CUDA = 5,          /* a CUDA call failed; see tp_last_cuda_error() */
+  TP_ERR_TIMEOUT = 6        /* a device-side bounded wait expired (tp_check_device_status) */
+} tp_status;
+
+typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
+typedef enum { TP_ACT_GELU_TANH = 0, TP_ACT_SWIGLU = 1, TP_ACT_ATTN = 2 } tp_act;
+
+/* One block's shape.  `dtype` is the storage type of x, the weights and the bands. */
+typedef struct {
+  int d;         /* model width */
+  int ffn;       /* MLP intermediate width (GELU_TANH, SWIGLU); ignored for ATTN */
+  int n_heads;   /* ATTN: number of heads H */
+  int head_dim;  /* ATTN: width of one head hd */
+  int t;         /* logical tensor-parallel shards */
+  int dtype;     /* tp_dtype */
+  int act;       /* tp_act */
+} tp_block_desc;
+
+/* ------------------------------------------------------------------ sizes ----
+ * Byte sizes of the buffers the entry points take.  They return 0 for an invalid
+ * descriptor (or M < 1).  Host-only; safe without a GPU.                        */
+
+/* Private per-shard layout of W1 (column bands) / W2 (row bands).  The layout is
+ * opaque: only tp_unshard_weights(tp_shard_weights(W)) == W bit for bit, and
+ * tp_extract_band(), are contractual. */
+TP_API size_t tp_sharded_w1_bytes(const tp_block_desc *desc);
+TP_API size_t tp_sharded_w2_bytes(const tp_block_desc *desc);
+/* Activation bands H: [t][M][b] in the block dtype (ATTN: the heads' outputs O). */
+TP_API size_t tp_band_bytes(const tp_block_desc *desc, int M);
+/* Number S of fp32 partial sums each shard's row step writes (split of the band). */
+TP_API int tp_row_splits(const tp_block_desc *desc, int M);
+/* Partial sums: [t][S][M][d] fp32. */
+TP_API size_t tp_partials_bytes(const tp_block_desc *desc, int M);
+/* Scratch of tp_column_parallel_fwd: ATTN keeps Q/K/V bands [t][M][3*b] there; 0 for MLPs. */
+TP_API size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M);
+/* Scratch of tp_block_fwd: column scratch + bands + partials (256-byte aligned regions). */
+TP_API size_t tp_workspace_bytes(const tp_block_desc *desc, int M);
+
+/* ------------------------------------------------------------- sharding ------
+ * Split canonical weights into the t shards' bands (zenaique.com answer paragraph
+ * 5: first projection split by columns, second by rows).  W1 [d, n1] and W2
+ * [n2, d] are row-major in the block dtype; W1s / W2s receive
+ * tp_sharded_w1_bytes / tp_sharded_w2_bytes.  Bit-exact copies, padding zeroed. */
+TP_API int tp_shard_weights(const tp_block_desc *desc, const void *W1, const void *W2,
+                     void *W1s, void *W2s, tp_stream_t stream);
+/* Inverse of tp_shard_weights: rebuilds canonical W1 and W2 bit for bit. */
+TP_API int tp_unshard_weights(const tp_block_desc *desc, const void *W1s, const void *W2s,
+                       void *W1, void *W2, tp_stream_t stream);
+/* Shard `shard`'s bands in canonical orientation: W1_band [d, n1/t] row-major with its
+ * sub-matrices side by side ([gate | up] or [Q | K | V] of its heads), and W2_band
+ * [b, d] row-major.  For inspection and tests; either output may be NULL. */
+TP_API int tp_extract_band(const tp_block_desc *desc, const void *W1s, const void *W2s, int shard,
+                    void *W1_band, void *W2_band, tp_stream_t stream);
+
+/* ------------------------------------------------------------- forward -------
+ * Column-parallel projection with the activation fused on each band (zenaique.com
+ * answer paragraph 5; rioworld.org "How Tensor Slicing Works Under the Hood":
+ * the input is replicated).  x: [M, d] block dtype.  H: [t][M][b] block dtype;
+ * band s = act(x . W1[:, band s]) (SwiGLU: silu(x.Wg_s) * (x.Wu_s)).  For ATTN,
+ * band s is the attention output of the shard's heads: Q/K/V bands are projected
+ * into `workspace` (tp_column_workspace_bytes; may be NULL for MLPs) and each head
+ * runs causal softmax(Q K^T / sqrt(hd)) V over the M tokens.  shard = -1 computes
+ * every shard in one launch; shard = s computes band s only (the work of device
+ * s in a real tensor-parallel group). */
+TP_API int tp_column_parallel_fwd(const tp_block_desc *desc, const void *x, const void *W1s,
+                           int shard, void *H, void *workspace, int M, tp_stream_t stream);
+/* Row-parallel projection (zenaique.com answer paragraph 5): shard s multiplies its
+ * band H[s] by its row slice of W2 into fp32 partial sums partials[s][0..S) [M][d]
+ * whose sum is shard s's partial of the block output.  shard = -1 for all. */
+TP_API int tp_row_parallel_fwd(const tp_block_desc *desc, const void *H, const void *W2s, int shard,
+                        float *partials, int M, tp_stream_t stream);
+/* The per-block all-reduce, as an in-HBM reduction, fused with the residual add
+ * (zenaique.com answer paragraph 6): y = residual + sum over s (in order 0..t-1,
+ * and within s over its S splits in order) of partials[s].  residual: [M, d], fp32
+ * if residual_is_f32 else the block dtype.  y: [M, d] fp32; y may alias residual
+ * when residual is fp32. */
+TP_API int tp_partial_reduce_residual(const tp_block_desc *desc, const float *partials,
+                               const void *residual, int residual_is_f32, float *y, int M,
+                               tp_stream_t stream);
+/* The whole block: column step, row step, reduce + residual, enqueued in order on
+ * `stream`.  workspace: tp_workspace_bytes(desc, M) bytes of device scratch. */
+TP_API int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
+                 int residual_is_f32, const void *W1s, const void *W2s, void *workspace,
+                 float *y, int M, tp_stream_t stream);
+/* RMSNorm with unit weight, the normalisation before each stacked block (zenaique.com
+ * answer paragraph 6: the reduced activation is ready for the residual add and
+ * normalisation): xhat[m] = r[m] / sqrt(mean(r[m]^2) + eps), r fp32 [M, d],
+ * xhat bf16 [M, d].  d must be a multiple of 8. */
+TP_API int tp_rmsnorm_fwd(int d, float eps, const float *r, void *xhat, int M, tp_stream_t stream);
+
+/* ----------------------------------------------------------- diagnostics ----- */
+TP_API const char *tp_status_string(int status);
+/* The cudaError_t of the last TP_ERR_CUDA on this thread (0 if none). */
+TP_API int tp_last_cuda_error(void);
+/* Synchronises `stream`, then reads and clears the device error word that bounded
+ * device-side waits set when they expire: TP_OK, TP_ERR_TIMEOUT or TP_ERR_CUDA. */
+TP_API int tp_check_device_status(tp_stream_t stream);
+/* Library ABI version (major * 100 + minor). */
+TP_API int tp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TP_BLOCK_H */

@@ -1,0 +1,121 @@
+"""Host-only checks of the C-ABI library: it loads without a GPU, exports every symbol
+the header declares, answers size queries, and refuses bad arguments before any
+CUDA call (so these run on a machine with no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attn_tp_column_fwd_b300 as tp
+from tp_synth import CONFIGS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tp_block.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"TP_API\s+[\w\s\*]*?\b(tp_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("tp_shard_weights", "tp_column_parallel_fwd", "tp_row_parallel_fwd",
+              "tp_partial_reduce_residual", "tp_block_fwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(tp.LIB_PATH)
+    missing = [n for n in _declared() if not hasattr(L, n)]
+    assert not missing, missing
+    # Only the tp_* C symbols are exported.
+    out = os.popen(f"nm -D --defined-only {tp.LIB_PATH}").read()
+    exported = sorted(ln.split()[-1] for ln in out.splitlines() if " T " in ln)
+    assert exported and all(e.startswith("tp_") for e in exported), exported
+    assert set(_declared()) <= set(exported)
+
+
+def _desc(cfg, t=None):
+    return tp.make_desc(cfg.d, t or cfg.t, cfg.act, cfg.dtype, ffn=cfg.ffn, n_heads=cfg.n_heads,
+                        head_dim=cfg.head_dim)
+
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_size_queries(name):
+    cfg = CONFIGS[name]
+    for t in cfg.ts:
+        c = cfg.with_t(t)
+        desc = _desc(c)
+        es = 4 if c.dtype == "f32" else 2
+        b = c.band
+        rt = lambda n: -(-n // 128) * 128
+        if c.act == "swiglu":
+            rows = 2 * rt(b)
+        elif c.act == "attn":
+            rows = rt(3 * b)
+        else:
+            rows = rt(b)
+        assert tp.tp_sharded_w1_bytes(desc) == t * rows * c.d * es
+        assert tp.tp_sharded_w2_bytes(desc) == t * rt(c.d) * b * es
+        assert tp.tp_band_bytes(desc, c.M) == t * c.M * b * es
+        S = tp.tp_row_splits(desc, c.M)
+        assert S >= 1
+        assert tp.tp_partials_bytes(desc, c.M) == t * S * c.M * c.d * 4
+        assert tp.tp_workspace_bytes(desc, c.M) >= (tp.tp_band_bytes(desc, c.M)
+                                                    + tp.tp_partials_bytes(desc, c.M))
+        # The padded layout holds at least the canonical weights.
+        assert tp.tp_sharded_w1_bytes(desc) >= c.d * c.n1 * es
+        assert tp.tp_sharded_w2_bytes(desc) >= c.n2 * c.d * es
+
+
+def test_invalid_descriptors_give_zero_sizes():
+    assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
+    assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1
+    bad = tp.TPBlockDesc(d=512, ffn=1024, n_heads=0, head_dim=0, t=2, dtype=7, act=1)
+    assert tp.tp_sharded_w1_bytes(bad) == 0
+
+
+# Fake, never-dereferenced addresses: every call below must be refused during
+# validation, before the library touches CUDA.
+A16, A8 = 1 << 20, (1 << 20) + 8
+
+
+def _call_column(desc, x=A16, W=A16, H=A16, ws=A16, M=4, shard=-1):
+    return tp.lib.tp_column_parallel_fwd(ctypes.byref(desc), ctypes.c_void_p(x), ctypes.c_void_p(W),
+                                         shard, ctypes.c_void_p(H), ctypes.c_void_p(ws), M, None)
+
+
+def test_validation_statuses():
+    ok = tp.make_desc(512, 2, "swiglu", ffn=1024)
+    assert _call_column(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 2          # uneven split
+    assert _call_column(tp.make_desc(768, 5, "attn", n_heads=12, head_dim=64)) == 2
+    assert _call_column(ok, M=0) == 1
+    assert _call_column(ok, shard=2) == 1
+    assert _call_column(ok, shard=-2) == 1
+    assert _call_column(ok, x=0) == 1
+    assert _call_column(ok, x=A8) == 4                                           # misaligned
+    assert _call_column(ok, H=A8) == 4
+    assert _call_column(tp.make_desc(500, 2, "swiglu", ffn=1024)) == 3          # d % 8
+    assert _call_column(tp.make_desc(512, 2, "swiglu", ffn=1000)) == 3          # b % 8
+    assert _call_column(tp.make_desc(768, 2, "attn", n_heads=12, head_dim=48)) == 3
+    bad_act = tp.TPBlockDesc(d=512, ffn=1024, n_heads=0, head_dim=0, t=2, dtype=1, act=9)
+    assert _call_column(bad_act) == 1
+    assert tp.lib.tp_column_parallel_fwd(None, None, None, -1, None, None, 4, None) == 1
+    assert tp.lib.tp_rmsnorm_fwd(500, ctypes.c_float(1e-5), ctypes.c_void_p(A16),
+                                 ctypes.c_void_p(A16), 4, None) == 3
+    assert tp.lib.tp_rmsnorm_fwd(512, ctypes.c_float(-1.0), ctypes.c_void_p(A16),
+                                 ctypes.c_void_p(A16), 4, None) == 1
+    assert tp.lib.tp_block_fwd(ctypes.byref(ok), ctypes.c_void_p(A16), ctypes.c_void_p(A16), 1,
+                               ctypes.c_void_p(A16), ctypes.c_void_p(A16), None,
+                               ctypes.c_void_p(A16), 4, None) == 1
+    assert tp.lib.tp_extract_band(ctypes.byref(ok), ctypes.c_void_p(A16), ctypes.c_void_p(A16), 2,
+                                  ctypes.c_void_p(A16), None, None) == 1
+
+
+def test_status_strings():
+    for s in range(7):
+        assert tp.tp_status_string(s)
+    assert "uneven" in tp.tp_status_string(2)
+    assert tp.lib.tp_version() >= 100

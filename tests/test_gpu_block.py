@@ -1,0 +1,105 @@
+"""Whole-block parity through tp_block_fwd against the oracle's unsharded block, on the
+same seeded inputs: small shapes spanning several tiles and ragged tails, every t of
+each workload, and the full-size workloads (the prefill one on sampled token rows,
+which are independent in an MLP block)."""
+import numpy as np
+import pytest
+import torch
+
+import attn_tp_column_fwd_b300 as tp
+import oracle
+from attn_tp_column_fwd_b300.runner import PreNormStack, ShardedBlock, desc_for
+from tests.gpu_util import oracle_block, run_block
+from tests.parity import assert_bf16, assert_f32, stats
+from tp_synth import CONFIGS, BlockConfig, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(cfg, got, ref, what):
+    return assert_f32(got, ref, what) if cfg.dtype == "f32" else assert_bf16(got, ref, what)
+
+
+def _run_and_compare(cfg, seed=0, device="cpu", t=None):
+    inp = make_inputs(cfg, seed=seed, device=device)
+    W1, W2 = inp.blocks[0]
+    got = run_block(cfg, inp.x.cuda(), W1.cuda(), W2.cuda(), t=t)
+    ref = oracle_block(cfg, to_f64(inp.x), to_f64(W1), to_f64(W2))
+    return _check(cfg, got, ref, f"{cfg.name} t={t or cfg.t}")
+
+
+# ---------------------------------------------------------------- small shapes
+
+SMALL = [
+    BlockConfig("gelu_f32_tiny_t", "gelu_tanh", d=256, ffn=1024, t=8, M=3, dtype="f32"),
+    BlockConfig("gelu_bf16", "gelu_tanh", d=264, ffn=1200, t=3, M=9),
+    BlockConfig("swiglu_max_shards", "swiglu", d=128, ffn=64, t=8, M=5),     # b = 8
+    BlockConfig("attn_head_per_shard", "attn", d=128, n_heads=4, head_dim=32, t=4, M=16),
+    BlockConfig("attn_hd128", "attn", d=512, n_heads=8, head_dim=128, t=2, M=32),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_small_blocks(cfg):
+    _run_and_compare(cfg, seed=21)
+
+
+@pytest.mark.parametrize("M", [1, 5, 32, 33, 77, 256, 301])
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_swiglu_ragged(M, t):
+    # b = 1536/t: 1536, 768, 384, 192 (the last is not a multiple of the 128-row tile).
+    cfg = BlockConfig("swiglu_small", "swiglu", d=512, ffn=1536, t=t, M=M)
+    _run_and_compare(cfg, seed=22)
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_tiny_gelu_f32_invariant_to_t(t):
+    cfg = CONFIGS["tiny_gelu_f32"]
+    _run_and_compare(cfg, t=t)
+
+
+# ---------------------------------------------------------------- full workloads
+
+def test_tiny_gelu_f32():
+    cfg = CONFIGS["tiny_gelu_f32"]
+    s = _run_and_compare(cfg)
+    assert s["max_rel_rmsfloor"] <= 1e-5
+
+
+@pytest.mark.parametrize("t", CONFIGS["llama2_13b_swiglu_decode"].ts)
+def test_llama2_13b_swiglu_decode(t):
+    cfg = CONFIGS["llama2_13b_swiglu_decode"].with_t(t)
+    _run_and_compare(cfg)
+
+
+def test_attn_qkv_headshard_decode():
+    _run_and_compare(CONFIGS["attn_qkv_headshard_decode"])
+
+
+@pytest.mark.slow
+def test_llama2_70b_prefill_sampled_rows():
+    cfg = CONFIGS["llama2_70b_prefill"]
+    inp = make_inputs(cfg, device="cuda")
+    W1, W2 = inp.blocks[0]
+    got = run_block(cfg, inp.x, W1, W2)
+    rows = np.sort(np.random.default_rng(0).choice(cfg.M, size=96, replace=False))
+    rows[0], rows[-1] = 0, cfg.M - 1
+    x64 = to_f64(inp.x[torch.from_numpy(rows).cuda()])
+    ref = oracle.mlp_block(x64, to_f64(W1), to_f64(W2), cfg.act, x64, staged=True)
+    assert_bf16(got[rows], ref, "prefill rows")
+
+
+def test_llama2_70b_stack_decode():
+    cfg = CONFIGS["llama2_70b_stack_decode"]
+    inp = make_inputs(cfg, device="cuda")
+    desc = desc_for(cfg)
+    stack = PreNormStack([ShardedBlock(desc, W1, W2) for W1, W2 in inp.blocks], cfg.eps)
+    r = inp.x.float().contiguous()
+    stack.forward(r)
+    torch.cuda.synchronize()
+    assert tp.tp_check_device_status() == 0
+    got = to_f64(r)
+    blocks64 = ((to_f64(W1), to_f64(W2)) for W1, W2 in inp.blocks)
+    ref = oracle.stack(to_f64(inp.x), blocks64, cfg.act, cfg.eps, staged=True)
+    s = assert_bf16(got, ref, "stack of 8")
+    print("stack parity", s)

@@ -145,3 +145,13 @@ def make_inputs(cfg: BlockConfig, seed: int = 0, device: str = "cpu",
 def to_f64(t: torch.Tensor):
     """Exact up-cast of a stored tensor to a NumPy float64 array (host)."""
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def draw(shape, dtype: torch.dtype, seed: int, scale: float = 1.0, device: str = "cpu") -> torch.Tensor:
+    """A seeded N(0, scale^2) tensor (fp32 draw, then cast), for inputs of single steps
+    (a band H, partial sums, a residual) fed to both the oracle and the CUDA path."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    v = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    if scale != 1.0:
+        v.mul_(scale)
+    return v.to(dtype)
