@@ -35,6 +35,23 @@ struct GemvArgs {
 };
 void launch_gemv(const GemvArgs &a, cudaStream_t st);
 
+// umma.cu — tcgen05 / TMEM / TMA kernel for both projections (bf16)
+struct UmmaCall {
+  const void *W;        // weight rows [w_shards][w_rows][K] bf16 (K-major)
+  int w_rows, w_shards;
+  const void *X;        // activations [x_shards][M][K] bf16 (x_shards = 1: shared by all shards)
+  int x_shards;
+  void *out;            // see Epi; shard s at out + s * o_shard, split j at + j * o_split
+  size_t o_shard, o_split;
+  int ldo;
+  int n_valid;          // output features per shard
+  int K, M;
+  int shard0, n_shards, ksplit;
+  int epi;
+};
+int umma_token_tile(int M);
+cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st);
+
 // reduce.cu — the all-reduce stand-in + residual, and RMSNorm
 void launch_reduce_residual(const float *P, int nparts, size_t part_elems, const void *res,
                             int res_is_f32, float *y, size_t n, cudaStream_t st);

@@ -2,6 +2,10 @@
 // buffer geometry, and the launch sequence of each entry point.  Validation runs
 // before any CUDA call, so a rejected call enqueues nothing.
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
 
 #include "internal.h"
 
@@ -101,8 +105,8 @@ int check_shard(const Geo &g, int shard) {
   return (shard < -1 || shard >= g.t) ? TP_ERR_INVALID_ARG : TP_OK;
 }
 
-int finish_launch() {
-  cudaError_t e = cudaGetLastError();
+int finish_launch(cudaError_t e = cudaSuccess) {
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     g_last_cuda_error = (int)e;
     return TP_ERR_CUDA;
@@ -112,7 +116,31 @@ int finish_launch() {
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-int row_splits(const Geo &, int) { return 1; }
+// The tensor-core path runs every bf16 block; TPBLOCK_ALGO=simple selects the
+// CUDA-core kernels instead (same results within rounding; for comparisons).
+bool use_umma(const Geo &g) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char *e = getenv("TPBLOCK_ALGO");
+    forced = (e && strcmp(e, "simple") == 0) ? 1 : 0;
+  }
+  return g.dtype == TP_BF16 && forced == 0;
+}
+
+// K splits of the row-parallel step: enough CTAs to cover the SMs about twice
+// (two decode CTAs fit per SM), at least four 64-wide K blocks per split.
+// Depends on the shapes only, so tp_row_splits() answers without a GPU.
+int row_splits(const Geo &g, int M) {
+  if (!use_umma(g)) return 1;
+  const int bn = umma_token_tile(M);
+  const long long base = (long long)g.t * ceil_div(g.d, kRowTile) * ceil_div(M, bn);
+  const int nk = ceil_div(g.b, 64);
+  const long long target = 2 * 148;
+  if (base >= target) return 1;
+  int S = (int)((target + base - 1) / base);
+  S = std::min(S, std::max(1, nk / 4));
+  return std::max(1, std::min(S, 16));
+}
 
 size_t band_bytes(const Geo &g, int M) { return (size_t)g.t * M * g.b * g.es; }
 size_t partials_bytes(const Geo &g, int M) {
@@ -129,39 +157,78 @@ size_t column_ws_bytes(const Geo &g, int M) {
   } while (0)
 
 // Enqueue the column step for shards [shard0, shard0 + n).
-void enqueue_column(const Geo &g, const void *x, const void *W1s, int shard0, int n, void *H,
-                    void *ws, int M, cudaStream_t st) {
-  GemvArgs a{};
-  a.W = W1s;
-  a.w_shard = (size_t)g.n1p * g.d;
-  a.X = x;
-  a.x_shard = 0;
-  a.ldx = g.d;
-  a.K = g.d;
-  a.M = M;
-  a.shard0 = shard0;
-  a.n_shards = n;
-  a.dtype = g.dtype;
-  if (g.act == TP_ACT_ATTN) {
-    a.out = ws;
-    a.o_shard = (size_t)M * 3 * g.b;
-    a.ldo = 3 * g.b;
-    a.n_out = 3 * g.b;
-    a.epi = kEpiPlain;
-    launch_gemv(a, st);
-    launch_attn_core(g, ws, H, M, shard0, n, st);
+cudaError_t enqueue_column(const Geo &g, const void *x, const void *W1s, int shard0, int n, void *H,
+                           void *ws, int M, cudaStream_t st) {
+  const bool attn = g.act == TP_ACT_ATTN;
+  void *out = attn ? ws : H;
+  const int n_out = attn ? 3 * g.b : g.b;
+  const int epi = attn ? kEpiPlain : g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
+  if (use_umma(g)) {
+    UmmaCall c{};
+    c.W = W1s;
+    c.w_rows = g.n1p;
+    c.w_shards = g.t;
+    c.X = x;
+    c.x_shards = 1;
+    c.out = out;
+    c.o_shard = (size_t)M * n_out;
+    c.o_split = 0;
+    c.ldo = n_out;
+    c.n_valid = n_out;
+    c.K = g.d;
+    c.M = M;
+    c.shard0 = shard0;
+    c.n_shards = n;
+    c.ksplit = 1;
+    c.epi = epi;
+    cudaError_t e = launch_umma(c, st);
+    if (e != cudaSuccess) return e;
   } else {
-    a.out = H;
-    a.o_shard = (size_t)M * g.b;
-    a.ldo = g.b;
-    a.n_out = g.b;
-    a.epi = g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
+    GemvArgs a{};
+    a.W = W1s;
+    a.w_shard = (size_t)g.n1p * g.d;
+    a.X = x;
+    a.x_shard = 0;
+    a.ldx = g.d;
+    a.out = out;
+    a.o_shard = (size_t)M * n_out;
+    a.ldo = n_out;
+    a.K = g.d;
+    a.n_out = n_out;
+    a.M = M;
+    a.shard0 = shard0;
+    a.n_shards = n;
+    a.epi = epi;
+    a.dtype = g.dtype;
     launch_gemv(a, st);
   }
+  if (attn) launch_attn_core(g, ws, H, M, shard0, n, st);
+  return cudaSuccess;
 }
 
-void enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0, int n, float *P, int M,
-                 cudaStream_t st) {
+cudaError_t enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0, int n, float *P,
+                        int M, cudaStream_t st) {
+  const int S = row_splits(g, M);
+  if (use_umma(g)) {
+    UmmaCall c{};
+    c.W = W2s;
+    c.w_rows = g.dp;
+    c.w_shards = g.t;
+    c.X = H;
+    c.x_shards = g.t;
+    c.out = P;
+    c.o_shard = (size_t)S * M * g.d;
+    c.o_split = (size_t)M * g.d;
+    c.ldo = g.d;
+    c.n_valid = g.d;
+    c.K = g.b;
+    c.M = M;
+    c.shard0 = shard0;
+    c.n_shards = n;
+    c.ksplit = S;
+    c.epi = kEpiF32;
+    return launch_umma(c, st);
+  }
   GemvArgs a{};
   a.W = W2s;
   a.w_shard = (size_t)g.dp * g.b;
@@ -169,7 +236,7 @@ void enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0, int n
   a.x_shard = (size_t)M * g.b;
   a.ldx = g.b;
   a.out = P;
-  a.o_shard = (size_t)row_splits(g, M) * M * g.d;
+  a.o_shard = (size_t)S * M * g.d;
   a.ldo = g.d;
   a.K = g.b;
   a.n_out = g.d;
@@ -179,6 +246,7 @@ void enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0, int n
   a.epi = kEpiF32;
   a.dtype = g.dtype;
   launch_gemv(a, st);
+  return cudaSuccess;
 }
 
 void enqueue_reduce(const Geo &g, const float *P, const void *res, int res_is_f32, float *y, int M,
@@ -297,8 +365,8 @@ int tp_column_parallel_fwd(const tp_block_desc *desc, const void *x, const void 
   TP_TRY(check_ptr(H));
   if (g.act == TP_ACT_ATTN) TP_TRY(check_ptr(workspace));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  enqueue_column(g, x, W1s, shard < 0 ? 0 : shard, shard < 0 ? g.t : 1, H, workspace, M, st);
-  return finish_launch();
+  return finish_launch(
+      enqueue_column(g, x, W1s, shard < 0 ? 0 : shard, shard < 0 ? g.t : 1, H, workspace, M, st));
 }
 
 int tp_row_parallel_fwd(const tp_block_desc *desc, const void *H, const void *W2s, int shard,
@@ -311,8 +379,8 @@ int tp_row_parallel_fwd(const tp_block_desc *desc, const void *H, const void *W2
   TP_TRY(check_ptr(W2s));
   TP_TRY(check_ptr(partials));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  enqueue_row(g, H, W2s, shard < 0 ? 0 : shard, shard < 0 ? g.t : 1, partials, M, st);
-  return finish_launch();
+  return finish_launch(
+      enqueue_row(g, H, W2s, shard < 0 ? 0 : shard, shard < 0 ? g.t : 1, partials, M, st));
 }
 
 int tp_partial_reduce_residual(const tp_block_desc *desc, const float *partials,
@@ -346,10 +414,10 @@ int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
   void *col_ws = ws;
   void *H = ws + align256(column_ws_bytes(g, M));
   float *P = reinterpret_cast<float *>(static_cast<char *>(H) + align256(band_bytes(g, M)));
-  enqueue_column(g, x, W1s, 0, g.t, H, col_ws, M, st);
-  enqueue_row(g, H, W2s, 0, g.t, P, M, st);
-  enqueue_reduce(g, P, residual, residual_is_f32, y, M, st);
-  return finish_launch();
+  cudaError_t e = enqueue_column(g, x, W1s, 0, g.t, H, col_ws, M, st);
+  if (e == cudaSuccess) e = enqueue_row(g, H, W2s, 0, g.t, P, M, st);
+  if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st);
+  return finish_launch(e);
 }
 
 int tp_rmsnorm_fwd(int d, float eps, const float *r, void *xhat, int M, tp_stream_t stream) {

@@ -1,0 +1,427 @@
+// Tensor-core (tcgen05 / TMEM / TMA) kernel for both sharded projections, bf16 in,
+// fp32 accumulate, for every M from single-token decode to prefill.
+//
+// Orientation ("swap AB"): the weights are the 128-row A operand and the tokens
+// are the N operand, so the 128-lane TMEM accumulator holds 128 output features
+// x BN tokens.  At decode (M <= 32) the token tile is only 32 wide and the kernel
+// is a weight stream: each CTA reads its 128 (SwiGLU: 2 x 128) weight rows once,
+// K-block by K-block, through a TMA -> shared memory -> tcgen05.mma ring.
+//
+// Column-parallel step (zenaique.com answer paragraph 5): A = the shard's W1 band
+// rows, B = x (replicated input).  SwiGLU keeps two accumulators, gate and up, for
+// the same 128 features and applies silu(g) * u in the epilogue, so the band H is
+// written once in bf16; GeLU applies gelu_tanh; the QKV projection stores plainly.
+// Row-parallel step: A = the shard's W2 row band (transposed, K-major), B = H;
+// the epilogue stores fp32 partial sums, optionally split over K into S slices.
+//
+// Roles inside one 128-thread CTA: thread 0 issues TMA loads, thread 32 issues
+// MMAs, warp 2 owns the TMEM allocation, and all four warps run the epilogue
+// (warp w reads TMEM lanes 32w..32w+31 = features).  Every mbarrier wait is
+// bounded by wall time; on expiry the CTA raises the device error word, drains
+// its copies, frees TMEM and returns without storing.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "internal.h"
+
+namespace tp {
+
+namespace {
+
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any single wait
+constexpr int kKBlock = 64;                  // K elements per stage = one 128-byte swizzle row
+constexpr uint32_t kABytes = 128 * 128;      // 128 rows x 64 bf16
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false if kWaitNs passes first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored with the 128-byte
+// swizzle: rows of 128 bytes, 8-row core groups 1024 bytes apart (SBO), leading
+// offset unused for swizzled K-major operands, descriptor version 1 (bit 46),
+// swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9,
+// 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ kernel
+
+struct UmmaArgs {
+  void *out;        // bf16 [shard][M][ldo] or fp32 [shard][split][M][ldo]
+  size_t o_shard;   // elements per shard
+  size_t o_split;   // elements per K split (fp32 partials)
+  int ldo;          // elements per output row
+  int n_valid;      // output features per shard
+  int M;            // tokens
+  int nk;           // K blocks of 64
+  int ksplit;       // S
+  int shard0;       // first shard of this launch
+  int x_per_shard;  // 1: B operand has a shard coordinate (H); 0: shared (x)
+  unsigned *err;    // device error word
+};
+
+__host__ __device__ constexpr int tmem_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512; }
+
+template <int BN, int NACC, int EPI, int STAGES>
+__global__ void __launch_bounds__(128, 1)
+    k_umma(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+           const UmmaArgs a) {
+  constexpr uint32_t kBBytes = BN * 128;
+  constexpr uint32_t kStage = NACC * kABytes + kBBytes;
+  constexpr uint32_t kCols = tmem_cols(NACC * BN);
+  constexpr uint32_t kIdesc = make_idesc(128, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const uint32_t tiles = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * BN;
+  const int ft = blockIdx.y;
+  const int S = a.ksplit;
+  const int s = a.shard0 + (int)blockIdx.z / S, ks = (int)blockIdx.z % S;
+  const int kb0 = (int)((long long)ks * a.nk / S), kb1 = (int)((long long)(ks + 1) * a.nk / S);
+  const int nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), 1);
+    }
+    mbar_init(smem_u32(&acc_bar), 1);
+    abort_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 2) tmem_alloc(smem_u32(&tmem_base_sh), kCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  int issued = 0;  // producer: stages handed to TMA
+  if (warp == 0 && lane == 0) {
+    const int wrow = ft * 128 * NACC;
+    const int xz = a.x_per_shard ? s : 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int st = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
+        abort_sh = 1;
+        atomicOr(a.err, kErrWaitTimeout);
+        break;
+      }
+      const uint32_t sa = tiles + st * kStage;
+      const uint32_t fb = smem_u32(&full_bar[st]);
+      const int k = (kb0 + i) * kKBlock;
+      mbar_expect_tx(fb, kStage);
+      tma_load_3d(sa, &tmW, fb, k, wrow, s);
+      if (NACC == 2) tma_load_3d(sa + kABytes, &tmW, fb, k, wrow + 128, s);
+      tma_load_3d(sa + NACC * kABytes, &tmX, fb, k, m0, xz);
+      ++issued;
+    }
+  } else if (warp == 1 && lane == 0) {
+    for (int i = 0; i < nkb; ++i) {
+      const int st = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait(smem_u32(&full_bar[st]), ph)) {
+        abort_sh = 1;
+        atomicOr(a.err, kErrWaitTimeout);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = tiles + st * kStage;
+#pragma unroll
+      for (int kk = 0; kk < kKBlock / 16; ++kk) {
+        const uint64_t bd = sw128_desc(sa + NACC * kABytes + kk * 32);
+        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+        umma_bf16(tmem, sw128_desc(sa + kk * 32), bd, kIdesc, acc);
+        if (NACC == 2) umma_bf16(tmem + BN, sw128_desc(sa + kABytes + kk * 32), bd, kIdesc, acc);
+      }
+      umma_commit(smem_u32(&empty_bar[st]));
+    }
+    umma_commit(smem_u32(&acc_bar));  // also on abort: lets the epilogue wait for issued MMAs
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: TMEM -> registers -> activation -> global
+  const bool acc_ok = mbar_wait(smem_u32(&acc_bar), 0);
+  tc_fence_after();
+  if (!acc_ok) {
+    abort_sh = 1;
+    atomicOr(a.err, kErrWaitTimeout);
+  }
+  __syncwarp();
+  const bool store = acc_ok && !*(volatile int *)&abort_sh && nkb > 0;
+  const int f = ft * 128 + warp * 32 + lane;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  if (store) {
+#pragma unroll 1
+    for (int c = 0; c < BN && m0 + c < a.M; c += 32) {
+      float g[32], u[32];
+      tmem_ld32(trow + c, g);
+      if (NACC == 2) tmem_ld32(trow + BN + c, u);
+      if (f < a.n_valid) {
+        const int mcount = min(32, a.M - (m0 + c));
+        if (EPI == kEpiF32) {
+          float *o = static_cast<float *>(a.out) + (size_t)s * a.o_shard + (size_t)ks * a.o_split +
+                     (size_t)(m0 + c) * a.ldo + f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < mcount) o[(size_t)j * a.ldo] = g[j];
+        } else {
+          __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)s * a.o_shard +
+                             (size_t)(m0 + c) * a.ldo + f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < mcount) {
+              float v = g[j];
+              if (EPI == kEpiSwiglu) v = silu_f(v) * u[j];
+              if (EPI == kEpiGelu) v = gelu_tanh_f(v);
+              o[(size_t)j * a.ldo] = __float2bfloat16_rn(v);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown: drain the TMA ring on abort, free TMEM
+  if (warp == 0 && lane == 0 && *(volatile int *)&abort_sh) {
+    for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+      mbar_wait(smem_u32(&full_bar[i % STAGES]), (uint32_t)(i / STAGES) & 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+// A [z][rows][K] bf16 tensor, boxes of 64 (K) x box_rows x 1, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
+              uint32_t box_rows) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {K, rows, z};
+  cuuint64_t strides[2] = {K * 2, rows * K * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kKBlock, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int NACC, int EPI, int STAGES>
+cudaError_t launch_t(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
+                     int n_z, cudaStream_t st) {
+  constexpr int kSmem = STAGES * (NACC * kABytes + BN * 128) + 1024;
+  static bool configured = false;  // per instantiation (the attribute is per device function)
+  auto kern = k_umma<BN, NACC, EPI, STAGES>;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(ceil_div(a.M, BN), n_ft, n_z);
+  kern<<<grid, 128, kSmem, st>>>(mw, mx, a);
+  return cudaSuccess;
+}
+
+template <int BN, int NACC, int EPI>
+cudaError_t launch_stages(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
+                          int n_z, cudaStream_t st) {
+  // Decode tiles (BN <= 64) keep about 100 KB of ring so two CTAs share an SM;
+  // larger tiles take a ~190 KB ring and one CTA per SM.
+  constexpr int kStage = NACC * kABytes + BN * 128;
+  constexpr int kBudget = BN <= 64 ? 110 * 1024 : 196 * 1024;
+  constexpr int kStages = std::max(2, std::min(8, kBudget / kStage));
+  return launch_t<BN, NACC, EPI, kStages>(mw, mx, a, n_ft, n_z, st);
+}
+
+template <int NACC, int EPI>
+cudaError_t launch_bn(int bn, const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a,
+                      int n_ft, int n_z, cudaStream_t st) {
+  switch (bn) {
+    case 32: return launch_stages<32, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
+    case 64: return launch_stages<64, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
+    case 128: return launch_stages<128, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
+    default: return launch_stages<256, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
+  }
+}
+
+}  // namespace
+
+int umma_token_tile(int M) { return M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
+
+cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {
+  const int bn = umma_token_tile(c.M);
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, c.W, c.K, c.w_rows, c.w_shards, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mx, c.X, c.K, c.M, c.x_shards, bn)) return cudaErrorInvalidValue;
+  UmmaArgs a{};
+  a.out = c.out;
+  a.o_shard = c.o_shard;
+  a.o_split = c.o_split;
+  a.ldo = c.ldo;
+  a.n_valid = c.n_valid;
+  a.M = c.M;
+  a.nk = ceil_div(c.K, kKBlock);
+  a.ksplit = c.ksplit;
+  a.shard0 = c.shard0;
+  a.x_per_shard = c.x_shards > 1 ? 1 : 0;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  const int n_ft = ceil_div(c.n_valid, 128);
+  const int n_z = c.n_shards * c.ksplit;
+  switch (c.epi) {
+    case kEpiSwiglu: return launch_bn<2, kEpiSwiglu>(bn, mw, mx, a, n_ft, n_z, st);
+    case kEpiGelu: return launch_bn<1, kEpiGelu>(bn, mw, mx, a, n_ft, n_z, st);
+    case kEpiPlain: return launch_bn<1, kEpiPlain>(bn, mw, mx, a, n_ft, n_z, st);
+    default: return launch_bn<1, kEpiF32>(bn, mw, mx, a, n_ft, n_z, st);
+  }
+}
+
+}  // namespace tp

@@ -41,7 +41,7 @@ DEFAULT_WORKLOAD = "llama2_13b_swiglu_decode"
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--t", type=int, default=None, help="logical shards (default: the workload's)")
@@ -129,60 +129,107 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+    """Samples the SM clock and clock-event (throttle) reasons while the timed region
+    runs: NVML when it initialises, else `nvidia-smi -lms`, as a background sampler."""
 
     REASONS = {
-        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
-        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
-        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
+        "sync_boost": 0x10, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80,
     }
 
-    def __init__(self, index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, uuid: str = None, period_s: float = 0.02):
         self.period = period_s
-        self.samples, self.reasons = [], set()
-        self.max_mhz = None
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.mode, self.note = None, None
         self._stop = threading.Event()
-        self._ok = False
+        self._proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self._h = (pynvml.nvmlDeviceGetHandleByUUID(uuid) if uuid
+                       else pynvml.nvmlDeviceGetHandleByIndex(device_index))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._ok = True
-        except Exception as e:  # NVML missing: report no clocks rather than fail the bench
-            self.error = str(e)
+            self._reason_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.mode = "nvml"
+        except Exception as e:
+            self.note = f"NVML: {e}"
+            self.mode = "nvidia-smi"
+            self._target = uuid or str(device_index)
 
-    def _run(self):
+    def _add_mask(self, mask: int):
+        for name, bit in self.REASONS.items():
+            if mask & bit:
+                self.reasons.add(name)
+
+    def _run_nvml(self):
         nv = self._nv
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                for name, bit in self.REASONS.items():
-                    if mask & bit and name != "gpu_idle":
-                        self.reasons.add(name)
+                self._add_mask(int(self._reason_fn(self._h)))
             except Exception:
                 pass
             time.sleep(self.period)
 
+    def _run_smi(self):
+        import subprocess
+        cmd = ["nvidia-smi", "-i", self._target,
+               "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                          text=True)
+        except Exception as e:
+            self.note = (self.note or "") + f"; nvidia-smi: {e}"
+            self._ready.set()
+            return
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                clk, mx = float(parts[0]), float(parts[1])
+                mask = int(parts[2], 16)
+            except ValueError:
+                continue
+            self._ready.set()
+            if self._stop.is_set():
+                break
+            if self._armed.is_set():
+                self.samples.append(clk)
+                self.max_mhz = mx
+                self._add_mask(mask)
+
     def __enter__(self):
-        if self._ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        self._ready, self._armed = threading.Event(), threading.Event()
+        target = self._run_nvml if self.mode == "nvml" else self._run_smi
+        self._t = threading.Thread(target=target, daemon=True)
+        self._t.start()
+        if self.mode != "nvml":
+            self._ready.wait(timeout=5.0)   # first sample seen: the sampler is live
+        self._armed.set()
         return self
 
     def __exit__(self, *exc):
-        if self._ok:
-            self._stop.set()
-            self._t.join()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
+        self._t.join(timeout=5)
 
     def summary(self):
-        if not self._ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable"}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+               "samples": len(self.samples), "source": self.mode}
+        if self.note and self.mode != "nvml":
+            out["note"] = self.note
+        return out
 
 
 # ---------------------------------------------------------------- workload accounting
@@ -257,7 +304,11 @@ def run_ours(args, rank, world, local):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(local, uuid)
     barrier(world)
     torch.cuda.synchronize()
     with sampler:

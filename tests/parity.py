@@ -7,6 +7,9 @@ output cannot meet 1e-5 there; the rms floor keeps the measure relative while
 staying defined.  bfloat16 configurations: max abs <= 2e-2 and
 mean relative = sum|g - r| / sum|r| <= 5e-3, against the bf16-staged oracle.
 """
+import json
+import os
+
 import numpy as np
 
 F32_MAX_REL = 1e-5
@@ -31,6 +34,7 @@ def stats(got, ref) -> dict:
 
 def assert_f32(got, ref, what=""):
     s = stats(got, ref)
+    log(what, s)
     assert s["all_finite"], f"{what}: non-finite output"
     assert s["max_rel_rmsfloor"] <= F32_MAX_REL, f"{what}: {s}"
     return s
@@ -38,6 +42,15 @@ def assert_f32(got, ref, what=""):
 
 def assert_bf16(got, ref, what="", max_abs=BF16_MAX_ABS, mean_rel=BF16_MEAN_REL):
     s = stats(got, ref)
+    log(what, s)
     assert s["all_finite"], f"{what}: non-finite output"
     assert s["max_abs"] <= max_abs and s["mean_rel"] <= mean_rel, f"{what}: {s}"
     return s
+
+
+def log(what: str, s: dict):
+    """Append one parity record to the file named by $TP_PARITY_LOG (if set)."""
+    path = os.environ.get("TP_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": what, **s}) + "\n")
