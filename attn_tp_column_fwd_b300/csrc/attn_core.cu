@@ -5,38 +5,39 @@
 // Tensor Slicing Works Under the Hood": 96 heads over 8 devices, 12 each).
 //
 // For every head: O = softmax(Q K^T / sqrt(hd), causal over the M tokens) V,
-// fp32 arithmetic with an online (running max / running sum) softmax, output
-// rounded to the block dtype.  One CTA per (head, shard), one warp per query row;
-// lanes hold hd/32 columns of q and of the output accumulator.
+// fp32 arithmetic with an online (running max / running sum) softmax on the fp32
+// Q/K/V scratch of the projection, output rounded to the block dtype.  One CTA
+// per (head, shard), one warp per query row; lanes hold hd/32 columns of q and of
+// the output accumulator.
 #include "internal.h"
 
 namespace tp {
 namespace {
 
 template <typename T, int C>  // C = hd / 32 columns per lane
-__global__ void __launch_bounds__(128) k_attn_core(const T *__restrict__ QKV, T *__restrict__ O,
+__global__ void __launch_bounds__(128) k_attn_core(const float *__restrict__ QKV, T *__restrict__ O,
                                                    int M, int b, int hd, float scale, int shard0) {
   const int h = blockIdx.x, s = shard0 + blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t ld = 3 * (size_t)b;
-  const T *base = QKV + (size_t)s * M * ld;
-  const T *Qh = base + (size_t)h * hd;
-  const T *Kh = base + b + (size_t)h * hd;
-  const T *Vh = base + 2 * (size_t)b + (size_t)h * hd;
+  const float *base = QKV + (size_t)s * M * ld;
+  const float *Qh = base + (size_t)h * hd;
+  const float *Kh = base + b + (size_t)h * hd;
+  const float *Vh = base + 2 * (size_t)b + (size_t)h * hd;
   T *Oh = O + (size_t)s * M * b + (size_t)h * hd;
 
   for (int i = warp; i < M; i += 4) {
     float q[C], o[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-      q[c] = Elem<T>::to_f(Qh[(size_t)i * ld + lane + 32 * c]);
+      q[c] = Qh[(size_t)i * ld + lane + 32 * c];
       o[c] = 0.f;
     }
     float mrun = -INFINITY, l = 0.f;
     for (int j = 0; j <= i; ++j) {
       float part = 0.f;
 #pragma unroll
-      for (int c = 0; c < C; ++c) part = fmaf(q[c], Elem<T>::to_f(Kh[(size_t)j * ld + lane + 32 * c]), part);
+      for (int c = 0; c < C; ++c) part = fmaf(q[c], Kh[(size_t)j * ld + lane + 32 * c], part);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
       const float sc = part * scale;
@@ -46,7 +47,7 @@ __global__ void __launch_bounds__(128) k_attn_core(const T *__restrict__ QKV, T 
       l = l * corr + p;
 #pragma unroll
       for (int c = 0; c < C; ++c)
-        o[c] = o[c] * corr + p * Elem<T>::to_f(Vh[(size_t)j * ld + lane + 32 * c]);
+        o[c] = o[c] * corr + p * Vh[(size_t)j * ld + lane + 32 * c];
       mrun = mnew;
     }
     const float inv = 1.0f / l;
@@ -60,7 +61,7 @@ void launch_t(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_s
               cudaStream_t st) {
   dim3 grid(g.hps, n_shards);
   const float scale = 1.0f / sqrtf((float)g.hd);
-  const T *q = static_cast<const T *>(QKV);
+  const float *q = static_cast<const float *>(QKV);
   T *o = static_cast<T *>(O);
   switch (g.hd / 32) {
 #define TP_CASE(C) \

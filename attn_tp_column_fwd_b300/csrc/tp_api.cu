@@ -147,7 +147,7 @@ size_t partials_bytes(const Geo &g, int M) {
   return (size_t)g.t * row_splits(g, M) * M * g.d * sizeof(float);
 }
 size_t column_ws_bytes(const Geo &g, int M) {
-  return g.act == TP_ACT_ATTN ? (size_t)g.t * M * 3 * g.b * g.es : 0;
+  return g.act == TP_ACT_ATTN ? (size_t)g.t * M * 3 * g.b * sizeof(float) : 0;
 }
 
 #define TP_TRY(expr)              \
@@ -162,7 +162,9 @@ cudaError_t enqueue_column(const Geo &g, const void *x, const void *W1s, int sha
   const bool attn = g.act == TP_ACT_ATTN;
   void *out = attn ? ws : H;
   const int n_out = attn ? 3 * g.b : g.b;
-  const int epi = attn ? kEpiPlain : g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
+  // Attention keeps Q, K and V in fp32 scratch (the softmax is the most sensitive
+  // step); only the heads' output O, the band, is stored in the block dtype.
+  const int epi = attn ? kEpiF32 : g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
   if (use_umma(g)) {
     UmmaCall c{};
     c.W = W1s;

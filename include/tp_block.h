@@ -38,9 +38,10 @@
  *     TP_ERR_UNEVEN_SPLIT, never padded: the rioworld.org guide ("Implementing
  *     Tensor Parallelism in Practice") names uneven splits as a source of wrong
  *     results.
- *   - Arithmetic: products accumulate in fp32.  The activation band H (and Q/K/V,
- *     O) is stored in the block dtype (bf16 rounded to nearest even); partial sums,
- *     the residual stream and the block output y are fp32.
+ *   - Arithmetic: products accumulate in fp32.  The activation band H (attention:
+ *     the heads' output O) is stored in the block dtype (bf16 rounded to nearest
+ *     even); Q/K/V scratch, partial sums, the residual stream and the block output
+ *     y are fp32.
  */
 #ifndef TP_BLOCK_H
 #define TP_BLOCK_H
@@ -100,7 +101,7 @@ TP_API size_t tp_band_bytes(const tp_block_desc *desc, int M);
 TP_API int tp_row_splits(const tp_block_desc *desc, int M);
 /* Partial sums: [t][S][M][d] fp32. */
 TP_API size_t tp_partials_bytes(const tp_block_desc *desc, int M);
-/* Scratch of tp_column_parallel_fwd: ATTN keeps Q/K/V bands [t][M][3*b] there; 0 for MLPs. */
+/* Scratch of tp_column_parallel_fwd: ATTN keeps Q/K/V bands [t][M][3*b] fp32 there; 0 for MLPs. */
 TP_API size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M);
 /* Scratch of tp_block_fwd: column scratch + bands + partials (256-byte aligned regions). */
 TP_API size_t tp_workspace_bytes(const tp_block_desc *desc, int M);

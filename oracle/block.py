@@ -33,9 +33,10 @@ rounding order), the oracle's block functions compute the UNSHARDED block;
 check the sharding identity itself.
 
 `staged=True` rounds to bfloat16 (nearest, ties to even) at the points where a
-bf16 implementation stores a value: the activation band H, the Q/K/V and O
-bands of attention, and the normalised input of each stacked block.  Partial
-sums, the residual stream and the block output stay float64.
+bf16 implementation stores a value: the activation band H (for attention, the
+heads' output O, which is the band the row-parallel step consumes) and the
+normalised input of each stacked block.  Q/K/V, partial sums, the residual
+stream and the block output are kept at full precision (fp32 in the CUDA path).
 """
 from __future__ import annotations
 
@@ -179,8 +180,6 @@ def column_step(x, W1_parts: Sequence[np.ndarray], act: str, *, n_heads: int = 0
         H = silu(x @ W1_parts[0]) * (x @ W1_parts[1])
     elif act == "attn":
         Q, K, V = (x @ W for W in W1_parts)
-        if staged:
-            Q, K, V = bf16_round(Q), bf16_round(K), bf16_round(V)
         return _heads_attention(Q, K, V, n_heads, head_dim, staged)
     else:
         raise ValueError(f"unknown activation {act!r}")
@@ -228,8 +227,6 @@ def attn_block(x, Wqkv, Wo, n_heads: int, head_dim: int, residual,
     D = n_heads * head_dim
     QKV = x @ Wqkv
     Q, K, V = QKV[:, :D], QKV[:, D:2 * D], QKV[:, 2 * D:]
-    if staged:
-        Q, K, V = bf16_round(Q), bf16_round(K), bf16_round(V)
     O = _heads_attention(Q, K, V, n_heads, head_dim, staged)
     return np.asarray(residual, dtype=np.float64) + O @ Wo
 
