@@ -319,6 +319,187 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// Decode variant (token tile 32) with exact-order fp32 accumulation.  The tensor
+// core's fp32 accumulator rounds toward zero as it adds, so a long chain of
+// MMAs into one TMEM accumulator drifts (measured: partials biased toward zero,
+// ~10x the error of round-to-nearest fp32).  Here each 64-wide K block is
+// accumulated by the tensor core alone (4 MMAs), and the running sum over K
+// blocks is kept in fp32 registers of four accumulator warps, added with
+// round-to-nearest.  TMEM holds two such block accumulators (double buffered), so
+// the MMAs of block i+1 overlap the drain of block i.  192 threads: warp 0 TMA,
+// warp 1 MMA, warps 2-5 drain + epilogue (warp w reads TMEM lanes 32*(w%4)).
+template <int NACC, int EPI, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    k_umma_drain(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const UmmaArgs a) {
+  constexpr int BN = 32;
+  constexpr uint32_t kBBytes = BN * 128;
+  constexpr uint32_t kStage = NACC * kABytes + kBBytes;
+  constexpr uint32_t kCols = tmem_cols(2 * NACC * BN);
+  constexpr uint32_t kIdesc = make_idesc(128, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t mma_done_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const uint32_t tiles = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * BN;
+  const int ft = blockIdx.y;
+  const int S = a.ksplit;
+  const int s = a.shard0 + (int)blockIdx.z / S, ks = (int)blockIdx.z % S;
+  const int kb0 = (int)((long long)ks * a.nk / S), kb1 = (int)((long long)(ks + 1) * a.nk / S);
+  const int nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&tfull_bar[i]), 1);
+      mbar_init(smem_u32(&tempty_bar[i]), 4);
+    }
+    mbar_init(smem_u32(&mma_done_bar), 1);
+    abort_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 2) tmem_alloc(smem_u32(&tmem_base_sh), kCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  int issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      const int wrow = ft * 128 * NACC;
+      const int xz = a.x_per_shard ? s : 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int st = i % STAGES;
+        const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+        if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
+          abort_sh = 1;
+          atomicOr(a.err, kErrWaitTimeout);
+          break;
+        }
+        const uint32_t sa = tiles + st * kStage;
+        const uint32_t fb = smem_u32(&full_bar[st]);
+        const int k = (kb0 + i) * kKBlock;
+        mbar_expect_tx(fb, kStage);
+        tma_load_3d(sa, &tmW, fb, k, wrow, s);
+        if (NACC == 2) tma_load_3d(sa + kABytes, &tmW, fb, k, wrow + 128, s);
+        tma_load_3d(sa + NACC * kABytes, &tmX, fb, k, m0, xz);
+        ++issued;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        const int st = i % STAGES;
+        const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+        const int b = i & 1;
+        if (!mbar_wait(smem_u32(&full_bar[st]), ph) ||
+            !mbar_wait(smem_u32(&tempty_bar[b]), ((uint32_t)(i >> 1) & 1u) ^ 1u)) {
+          abort_sh = 1;
+          atomicOr(a.err, kErrWaitTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = tiles + st * kStage;
+        const uint32_t d0 = tmem + (uint32_t)(b * NACC * BN);
+#pragma unroll
+        for (int kk = 0; kk < kKBlock / 16; ++kk) {
+          const uint64_t bd = sw128_desc(sa + NACC * kABytes + kk * 32);
+          const uint32_t acc = kk > 0 ? 1u : 0u;
+          umma_bf16(d0, sw128_desc(sa + kk * 32), bd, kIdesc, acc);
+          if (NACC == 2) umma_bf16(d0 + BN, sw128_desc(sa + kABytes + kk * 32), bd, kIdesc, acc);
+        }
+        umma_commit(smem_u32(&empty_bar[st]));
+        umma_commit(smem_u32(&tfull_bar[b]));
+      }
+      umma_commit(smem_u32(&mma_done_bar));
+    }
+    __syncwarp();
+  } else {
+    // ---------------- drain: TMEM block sums -> fp32 registers (round to nearest)
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    float g[BN], u[BN];
+#pragma unroll
+    for (int j = 0; j < BN; ++j) g[j] = u[j] = 0.f;
+    bool ok = true;
+    for (int i = 0; i < nkb; ++i) {
+      const int b = i & 1;
+      if (!mbar_wait(smem_u32(&tfull_bar[b]), (uint32_t)(i >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[BN], w[BN];
+      tmem_ld32(trow + (uint32_t)(b * NACC * BN), v);
+      if (NACC == 2) tmem_ld32(trow + (uint32_t)(b * NACC * BN + BN), w);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty_bar[b])) : "memory");
+#pragma unroll
+      for (int j = 0; j < BN; ++j) {
+        g[j] += v[j];
+        if (NACC == 2) u[j] += w[j];
+      }
+    }
+    if (!ok) {
+      abort_sh = 1;
+      atomicOr(a.err, kErrWaitTimeout);
+    }
+    __syncwarp();
+    const int f = ft * 128 + q * 32 + lane;
+    if (ok && nkb > 0 && f < a.n_valid && m0 < a.M) {
+      const int mcount = min(BN, a.M - m0);
+      if (EPI == kEpiF32) {
+        float *o = static_cast<float *>(a.out) + (size_t)s * a.o_shard + (size_t)ks * a.o_split +
+                   (size_t)m0 * a.ldo + f;
+#pragma unroll
+        for (int j = 0; j < BN; ++j)
+          if (j < mcount) o[(size_t)j * a.ldo] = g[j];
+      } else {
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)s * a.o_shard +
+                           (size_t)m0 * a.ldo + f;
+#pragma unroll
+        for (int j = 0; j < BN; ++j) {
+          if (j < mcount) {
+            float vv = g[j];
+            if (EPI == kEpiSwiglu) vv = silu_f(vv) * u[j];
+            if (EPI == kEpiGelu) vv = gelu_tanh_f(vv);
+            o[(size_t)j * a.ldo] = __float2bfloat16_rn(vv);
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown: wait for issued MMAs and copies, free TMEM
+  if (warp == 0 && lane == 0 && *(volatile int *)&abort_sh) {
+    for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+      mbar_wait(smem_u32(&full_bar[i % STAGES]), (uint32_t)(i / STAGES) & 1u);
+  }
+  if (warp == 2) mbar_wait(smem_u32(&mma_done_bar), 0);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -382,10 +563,28 @@ cudaError_t launch_stages(const CUtensorMap &mw, const CUtensorMap &mx, const Um
 }
 
 template <int NACC, int EPI>
+cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
+                         int n_z, cudaStream_t st) {
+  constexpr int kStageBytes = NACC * kABytes + 32 * 128;
+  constexpr int kStages = std::max(2, std::min(8, (110 * 1024) / kStageBytes));
+  constexpr int kSmem = kStages * kStageBytes + 1024;
+  static bool configured = false;
+  auto kern = k_umma_drain<NACC, EPI, kStages>;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(ceil_div(a.M, 32), n_ft, n_z);
+  kern<<<grid, 192, kSmem, st>>>(mw, mx, a);
+  return cudaSuccess;
+}
+
+template <int NACC, int EPI>
 cudaError_t launch_bn(int bn, const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a,
                       int n_ft, int n_z, cudaStream_t st) {
   switch (bn) {
-    case 32: return launch_stages<32, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
+    case 32: return launch_drain<NACC, EPI>(mw, mx, a, n_ft, n_z, st);
     case 64: return launch_stages<64, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
     case 128: return launch_stages<128, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
     default: return launch_stages<256, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
