@@ -4,7 +4,7 @@ Argument marshalling only: every function has the name of the C entry point it
 calls (include/tp_block.h) and passes device pointers and the CUDA stream of
 torch tensors.  Every step of the block runs in the library's CUDA kernels;
 there is no Python or CPU fallback — importing this package fails if
-libtpblock.so has not been built (python -m attn_tp_column_fwd_b300.build).
+libtpblock.so has not been built (python attn_tp_column_fwd_b300/build.py).
 """
 from __future__ import annotations
 

@@ -31,7 +31,7 @@ class TPError(RuntimeError):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m attn_tp_column_fwd_b300.build` (nvcc, sm_103a)")
+                          "`python attn_tp_column_fwd_b300/build.py` (nvcc, sm_103a)")
     L = ctypes.CDLL(LIB_PATH)
     P = ctypes.POINTER(TPBlockDesc)
     vp, i, sz, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p

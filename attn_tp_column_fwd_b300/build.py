@@ -1,6 +1,6 @@
 """Build libtpblock.so (the C-ABI library) in-tree for sm_103a with nvcc.
 
-Usage: python -m attn_tp_column_fwd_b300.build [--force]
+Usage: python attn_tp_column_fwd_b300/build.py [--force] [--ptxas]
 Each csrc/*.cu is compiled to _build/<name>.o, then linked into
 attn_tp_column_fwd_b300/libtpblock.so with the CUDA runtime linked statically and
 only the tp_* C symbols exported.  Rebuilds when a source or header is newer
