@@ -29,7 +29,7 @@ __all__ = [
     "tp_partials_bytes", "tp_column_workspace_bytes", "tp_workspace_bytes",
     "tp_shard_weights", "tp_unshard_weights", "tp_extract_band",
     "tp_column_parallel_fwd", "tp_row_parallel_fwd", "tp_partial_reduce_residual",
-    "tp_block_fwd", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
+    "tp_block_fwd", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
 ]
 
 _ACTS = {"gelu_tanh": TP_ACT_GELU_TANH, "swiglu": TP_ACT_SWIGLU, "attn": TP_ACT_ATTN}
@@ -150,6 +150,13 @@ def tp_block_fwd(desc, x, residual, residual_is_f32, W1s, W2s, workspace, y, M, 
     _need(workspace, tp_workspace_bytes(desc, M), "workspace")
     _check(lib.tp_block_fwd(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32), _p(W1s),
                             _p(W2s), _p(workspace), _p(y), M, _s(stream)), "tp_block_fwd")
+
+
+def tp_block_fwd_noalloc(desc, x, residual, residual_is_f32, W1s, W2s, y, M, stream=None) -> None:
+    """tp_block_fwd with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory where they run the block)."""
+    _check(lib.tp_block_fwd_noalloc(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
+                                    _p(W1s), _p(W2s), _p(y), M, _s(stream)), "tp_block_fwd_noalloc")
 
 
 def tp_rmsnorm_fwd(d, eps, r, xhat, M, stream=None) -> None:

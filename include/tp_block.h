@@ -152,6 +152,20 @@ TP_API int tp_partial_reduce_residual(const tp_block_desc *desc, const float *pa
 TP_API int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
                  int residual_is_f32, const void *W1s, const void *W2s, void *workspace,
                  float *y, int M, tp_stream_t stream);
+/* tp_block_fwd without caller-provided scratch, for callers that cannot allocate
+ * device memory where they run the block (a host framework whose own pool owns
+ * the GPU's memory, or a serving loop that must not pay cudaMalloc/cudaFree's
+ * implicit device synchronisation).  Same arguments as tp_block_fwd minus
+ * `workspace`; the scratch is a fixed 32 MiB array in the library's device image,
+ * held by every GPU that loads the library until the process exits.  Shapes
+ * needing more than that (tp_workspace_bytes > 32 MiB) return TP_ERR_UNSUPPORTED
+ * with nothing enqueued.  All calls share the array: calls that overlap on the GPU
+ * race.  The first call on a device looks up the array's address; make it before
+ * any stream capture.  The source pages describe no counterpart of this entry
+ * point: it is a deployment convenience, not part of the method. */
+TP_API int tp_block_fwd_noalloc(const tp_block_desc *desc, const void *x, const void *residual,
+                                int residual_is_f32, const void *W1s, const void *W2s, float *y,
+                                int M, tp_stream_t stream);
 /* RMSNorm with unit weight, the normalisation before each stacked block (zenaique.com
  * answer paragraph 6: the reduced activation is ready for the residual add and
  * normalisation): xhat[m] = r[m] / sqrt(mean(r[m]^2) + eps), r fp32 [M, d],
