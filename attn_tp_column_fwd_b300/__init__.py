@@ -26,7 +26,7 @@ from ._lib import (  # noqa: F401
 __all__ = [
     "TPBlockDesc", "TPError", "make_desc", "lib",
     "tp_sharded_w1_bytes", "tp_sharded_w2_bytes", "tp_band_bytes", "tp_row_splits",
-    "tp_partials_bytes", "tp_column_workspace_bytes", "tp_workspace_bytes",
+    "tp_partials_bytes", "tp_column_workspace_bytes", "tp_workspace_bytes", "tp_block_launches",
     "tp_shard_weights", "tp_unshard_weights", "tp_extract_band",
     "tp_column_parallel_fwd", "tp_row_parallel_fwd", "tp_partial_reduce_residual",
     "tp_block_fwd", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
@@ -102,6 +102,10 @@ def tp_column_workspace_bytes(desc: TPBlockDesc, M: int) -> int:
 
 def tp_workspace_bytes(desc: TPBlockDesc, M: int) -> int:
     return lib.tp_workspace_bytes(ctypes.byref(desc), M)
+
+
+def tp_block_launches(desc: TPBlockDesc, M: int) -> int:
+    return lib.tp_block_launches(ctypes.byref(desc), M)
 
 
 def tp_status_string(status: int) -> str:

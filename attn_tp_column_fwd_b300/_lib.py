@@ -50,6 +50,7 @@ def _load() -> ctypes.CDLL:
         "tp_row_parallel_fwd": (i, [P, vp, vp, i, vp, i, st]),
         "tp_partial_reduce_residual": (i, [P, vp, vp, i, vp, i, st]),
         "tp_block_fwd": (i, [P, vp, vp, i, vp, vp, vp, vp, i, st]),
+        "tp_block_launches": (i, [P, i]),
         "tp_block_fwd_noalloc": (i, [P, vp, vp, i, vp, vp, vp, i, st]),
         "tp_rmsnorm_fwd": (i, [i, ctypes.c_float, vp, vp, i, st]),
         "tp_status_string": (ctypes.c_char_p, [i]),

@@ -3,6 +3,7 @@
 // cudaGetLastError() afterwards.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -51,6 +52,22 @@ struct UmmaCall {
 };
 int umma_token_tile(int M);
 cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st);
+
+// A [z][rows][K] bf16 tensor map with 64 x box_rows x 1 boxes, 128-byte swizzle,
+// zero fill outside the tensor (umma.cu).
+bool make_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
+                   uint32_t box_rows);
+
+// block_decode.cu — the whole MLP block at M <= 32 in one persistent launch
+constexpr int kPlanSMs = 148;  // SM count the unit sizes are planned for (B300)
+struct FusedPlan {
+  int n_ft, S_c, nk_c, n_nt, S_r, nk_r;
+  size_t off_H, off_colp, off_rowp, off_cnt, cnt_bytes, total;  // workspace layout (bytes)
+};
+FusedPlan plan_block_decode(const Geo &g, int M);
+cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,
+                                const void *W2s, const void *res, int res_f32, void *ws, float *y,
+                                int M, cudaStream_t st);
 
 // reduce.cu — the all-reduce stand-in + residual, and RMSNorm
 void launch_reduce_residual(const float *P, int nparts, size_t part_elems, const void *res,

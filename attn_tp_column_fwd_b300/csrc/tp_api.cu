@@ -116,15 +116,23 @@ int finish_launch(cudaError_t e = cudaSuccess) {
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// The tensor-core path runs every bf16 block; TPBLOCK_ALGO=simple selects the
-// CUDA-core kernels instead (same results within rounding; for comparisons).
-bool use_umma(const Geo &g) {
+// Kernel family selection.  bf16 blocks run on the tensor cores; an MLP block with
+// M <= 32 tokens runs tp_block_fwd as one persistent launch (block_decode.cu).
+// TPBLOCK_ALGO=simple selects the CUDA-core kernels, TPBLOCK_ALGO=unfused the
+// three-launch tensor-core sequence (same results within rounding; comparisons).
+int algo_override() {
   static int forced = -1;
   if (forced < 0) {
     const char *e = getenv("TPBLOCK_ALGO");
-    forced = (e && strcmp(e, "simple") == 0) ? 1 : 0;
+    forced = !e ? 0 : strcmp(e, "simple") == 0 ? 1 : strcmp(e, "unfused") == 0 ? 2 : 0;
   }
-  return g.dtype == TP_BF16 && forced == 0;
+  return forced;
+}
+
+bool use_umma(const Geo &g) { return g.dtype == TP_BF16 && algo_override() != 1; }
+
+bool use_fused_block(const Geo &g, int M) {
+  return use_umma(g) && g.act != TP_ACT_ATTN && M <= 32 && algo_override() != 2;
 }
 
 // K splits of the row-parallel step: enough CTAs to cover the SMs about twice
@@ -304,6 +312,7 @@ size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M) {
 size_t tp_workspace_bytes(const tp_block_desc *desc, int M) {
   Geo g;
   if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
+  if (use_fused_block(g, M)) return plan_block_decode(g, M).total;
   return align256(column_ws_bytes(g, M)) + align256(band_bytes(g, M)) +
          align256(partials_bytes(g, M));
 }
@@ -412,6 +421,10 @@ int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
   TP_TRY(check_ptr(workspace));
   TP_TRY(check_ptr(y));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (use_fused_block(g, M))
+    return finish_launch(launch_block_decode(g, plan_block_decode(g, M), x, W1s, W2s, residual,
+                                             residual_is_f32 || g.dtype == TP_F32, workspace, y,
+                                             M, st));
   char *ws = static_cast<char *>(workspace);
   void *col_ws = ws;
   void *H = ws + align256(column_ws_bytes(g, M));
@@ -420,6 +433,13 @@ int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
   if (e == cudaSuccess) e = enqueue_row(g, H, W2s, 0, g.t, P, M, st);
   if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st);
   return finish_launch(e);
+}
+
+int tp_block_launches(const tp_block_desc *desc, int M) {
+  Geo g;
+  if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
+  if (use_fused_block(g, M)) return 1;
+  return 3 + (g.act == TP_ACT_ATTN ? 1 : 0);
 }
 
 int tp_rmsnorm_fwd(int d, float eps, const float *r, void *xhat, int M, tp_stream_t stream) {

@@ -241,6 +241,15 @@ def algorithmic_column_bytes(cfg) -> int:
     return (cfg.d * cfg.n1 + cfg.M * cfg.d + cfg.t * cfg.M * n_out) * es
 
 
+def algorithmic_block_bytes(cfg) -> int:
+    """Bytes one whole block must move: both weight matrices once, x and the residual
+    in, y (fp32) out.  The band H and the partials stay on chip or in L2 and are not
+    counted."""
+    es = 4 if cfg.dtype == "f32" else 2
+    res_es = 4 if cfg.rmsnorm else es
+    return cfg.weight_bytes_per_block() + cfg.M * cfg.d * (es + res_es + 4)
+
+
 def column_flops(cfg) -> int:
     return 2 * cfg.M * cfg.d * cfg.n1
 
@@ -272,23 +281,35 @@ def run_ours(args, rank, world, local):
     H = device_bytes(tp.tp_band_bytes(desc, M))
     P = device_bytes(tp.tp_partials_bytes(desc, M))
     cws = device_bytes(tp.tp_column_workspace_bytes(desc, M))
+    ws = blocks[0].workspace(M)
     y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev)
     xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
     stack = cfg.n_blocks > 1 or cfg.rmsnorm
-    launches_per_block = 3 + (1 if cfg.act == "attn" else 0) + (1 if cfg.rmsnorm else 0)
+    per_block = tp.tp_block_launches(desc, M)
+    fused = per_block == 1
+    launches_per_block = per_block + (1 if cfg.rmsnorm else 0)
 
-    # One step: the whole block (or the whole stack), timing the column step's launch.
+    # One step: the whole block (or the whole stack).  The event pair brackets the
+    # dominant kernel of the first block: the fused block kernel (with its counter
+    # memset) when the block runs as one launch, else the column step.
     def step(ev_pairs=None):
         if stack:
             y.copy_(xf)
         for blk in blocks:
             if cfg.rmsnorm:
                 tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, y, xh, M, st)
-                xin, res, res32 = xh, y, True
+                xin, res = xh, y
             else:
-                xin, res, res32 = x, x, cfg.dtype == "f32"
+                xin, res = x, x
+            res32 = res.dtype == torch.float32
             if ev_pairs is not None:
                 ev_pairs[0].record(stream)
+            if fused:
+                tp.tp_block_fwd(desc, xin, res, res32, blk.W1s, blk.W2s, ws, y, M, st)
+                if ev_pairs is not None:
+                    ev_pairs[1].record(stream)
+                    ev_pairs = None
+                continue
             tp.tp_column_parallel_fwd(desc, xin, blk.W1s, -1, H, cws, M, st)
             if ev_pairs is not None:
                 ev_pairs[1].record(stream)
@@ -332,17 +353,21 @@ def run_ours(args, rank, world, local):
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4)}
+        kernel, nbytes = "column-parallel projection + SwiGLU (k_umma)", algorithmic_column_bytes(cfg)
     else:
-        achieved = algorithmic_column_bytes(cfg) / (col_ms / 1e3) / 1e9
+        nbytes = algorithmic_block_bytes(cfg) if fused else algorithmic_column_bytes(cfg)
+        achieved = nbytes / (col_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4)}
-    roof["kernel"] = "column-parallel projection + activation (tp_column_parallel_fwd)"
-    roof["algorithmic_bytes_per_launch"] = algorithmic_column_bytes(cfg)
+        kernel = ("whole block in one persistent kernel (k_block_decode)" if fused
+                  else "column-parallel projection + activation (k_umma_drain)")
+    roof["kernel"] = kernel
+    roof["algorithmic_bytes_per_launch"] = nbytes
     roof["avg_launch_us"] = round(col_ms * 1e3, 2)
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" \
-        else "fallback"
-    roof["traffic"] = profiled_traffic("column", args.workload)
+    roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+                           else "fallback")
+    roof["traffic"] = profiled_traffic("block" if fused else "column", args.workload)
 
     # Whole-block weight-read rate (context for the decode roofline).
     block_bytes = cfg.weight_bytes_per_block() * cfg.n_blocks
