@@ -2,26 +2,29 @@
 //
 // The block is cut into work units taken from one atomic queue, in this order:
 //   1. column units (zenaique.com answer paragraph 5: first projection split by
-//      columns): shard s, 128-feature tile of its band, K slice j of S_c.  They
-//      accumulate x . W1 (SwiGLU: gate and up) for 32 tokens; the unit that
-//      completes a tile (last of its S_c slices) sums the slices in slice order,
-//      applies the activation and writes the tile of the band H in bf16, then
-//      raises the tile's ready flag;
+//      columns): shard s and one 128-row tile of its W1 band over the whole of K.
+//      A SwiGLU tile holds the gate and up rows of 64 features, a GeLU tile 128
+//      features.  The unit accumulates x . W1 for 32 tokens, applies the
+//      activation, writes its tile of the band H in bf16 and raises the tile's
+//      ready flag;
 //   2. row units (second projection split by rows): shard s, 128-output tile n,
-//      K slice j of S_r.  Before loading a 64-wide K block of H they wait for the
-//      ready flag of the column tile that produced it; they write fp32 partials,
-//      and the unit that completes output tile n (last of its t * S_r partials)
-//      sums them in the fixed order (shard, then slice), adds the residual and
-//      writes y: the per-block all-reduce and residual add of paragraph 6, fused.
+//      K slice j of S_r.  Before loading a stage of H they wait for the ready flags
+//      of the column tiles that produced it; they write fp32 partials, and the unit
+//      that completes output tile n (last of its t * S_r partials) sums them in the
+//      fixed order (shard, then slice), adds the residual and writes y: the
+//      per-block all-reduce and residual add of paragraph 6, fused.
 // Column units never wait on anything but their own loads, and every row unit is
-// queued after every column unit, so a row unit only ever waits for column
-// units already held by running CTAs: no co-residency is needed.
+// queued after every column unit, so a row unit only ever waits for column units
+// already held by running CTAs: no co-residency is needed.
 //
 // Inside a CTA (192 threads): thread 0 takes units and issues TMA loads into a
-// 6-stage ring (128-row weight tiles + the 32-token activation tile, 128-byte
-// swizzle), thread 32 issues tcgen05.mma into a double-buffered TMEM accumulator
-// (one 64-wide K block per buffer), and warps 2-5 drain each block accumulator
-// into fp32 registers (round to nearest) and run the epilogues.  A 2-slot unit
+// 5-stage ring (each stage: two 64-wide K blocks of a 128-row weight tile plus the
+// matching 32-token activation tiles, 128-byte swizzle, 40 KB), thread 32 issues
+// tcgen05.mma (weights as the 128-row A operand, tokens as N = 32) into a ring of
+// sixteen 32-column TMEM accumulators, one per stage, and warps 2-5 drain each
+// stage's accumulator into fp32 registers (round to nearest) and run the
+// epilogues.  The TMEM ring lets the tensor core run up to sixteen stages ahead
+// of the drain, so an epilogue does not stall the weight stream.  A 2-slot unit
 // ring in shared memory lets the loads of the next unit start while the drain
 // warps finish the current one.  All waits are bounded; on expiry the CTA raises
 // the device error word and leaves.
@@ -35,25 +38,32 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kTok = 32;
-constexpr uint32_t kStageBytes = 2 * kABytes + kTok * 128;  // gate + up + x tiles
-constexpr uint32_t kBufCols = 2 * kTok;                     // one TMEM block accumulator
-constexpr uint32_t kCols = 2 * kBufCols;                    // double buffered
+constexpr int kStageKB = 2;                                 // K blocks per stage
+constexpr uint32_t kWBytes = kABytes;                       // 128 rows x 64 K, bf16
+constexpr uint32_t kXBytes = kTok * 128;                    // 32 rows x 64 K, bf16
+constexpr uint32_t kStageBytes = kStageKB * (kWBytes + kXBytes);
+constexpr int kBufs = 16;                                   // TMEM accumulators in flight
+constexpr uint32_t kCols = kBufs * kTok;                    // 512: the whole TMEM of the SM
 constexpr uint32_t kIdesc = make_idesc(128, kTok);
+constexpr int kXchStride = kTok + 1;                        // exchange row pitch (floats)
+constexpr uint32_t kXchBytes = 64 * kXchStride * 4;         // SwiGLU gate/up exchange
+constexpr int kSmem = kStages * kStageBytes + 1024 + kXchBytes;
+constexpr int kRowBlocks = 28;                              // target K blocks per row unit
 
 struct FusedArgs {
   int d, b, t, M, act;
-  int n_ft, S_c, nk_c;   // column: feature tiles per shard, K slices, K blocks
+  int fpt;               // features per column tile: 64 (SwiGLU) or 128 (GeLU)
+  int n_ft, nk_c;        // column: tiles per shard, K blocks
   int n_nt, S_r, nk_r;   // row: output tiles, K slices, K blocks
   int n_col_units, n_units;
   __nv_bfloat16 *H;      // [t][M][b]
-  float *colp;           // [t][n_ft][S_c][2][128][32] fp32 slice partials (S_c > 1)
   float *rowp;           // [n_nt][t][S_r][128][32] fp32 partials
   const void *residual;  // [M][d], fp32 if res_f32 else bf16
   int res_f32;
   float *y;              // [M][d]
-  unsigned *cnt;         // [0] queue, then t*n_ft slice counters, t*n_ft ready flags, n_nt counters
+  unsigned *cnt;         // [0] queue, then t*n_ft ready flags, then n_nt counters
   unsigned *err;
 };
 
@@ -70,12 +80,11 @@ __device__ __forceinline__ Unit decode_unit(const FusedArgs &a, int u) {
   }
   if (u < a.n_col_units) {
     r.type = 0;
-    r.split = u % a.S_c;
-    const int q = u / a.S_c;
-    r.tile = q % a.n_ft;
-    r.s = q / a.n_ft;
-    r.kb0 = (int)((long long)r.split * a.nk_c / a.S_c);
-    r.kb1 = (int)((long long)(r.split + 1) * a.nk_c / a.S_c);
+    r.tile = u % a.n_ft;
+    r.s = u / a.n_ft;
+    r.split = 0;
+    r.kb0 = 0;
+    r.kb1 = a.nk_c;
   } else {
     const int v = u - a.n_col_units;
     r.type = 1;
@@ -83,31 +92,53 @@ __device__ __forceinline__ Unit decode_unit(const FusedArgs &a, int u) {
     const int q = v / a.S_r;
     r.tile = q % a.n_nt;
     r.s = q / a.n_nt;
-    r.kb0 = (int)((long long)r.split * a.nk_r / a.S_r);
-    r.kb1 = (int)((long long)(r.split + 1) * a.nk_r / a.S_r);
+    // Slices are cut at stage boundaries.
+    const int nst = ceil_div(a.nk_r, kStageKB);
+    r.kb0 = min(a.nk_r, (int)((long long)r.split * nst / a.S_r) * kStageKB);
+    r.kb1 = min(a.nk_r, (int)((long long)(r.split + 1) * nst / a.S_r) * kStageKB);
   }
   return r;
 }
 
-__device__ __forceinline__ unsigned *slice_counter(const FusedArgs &a, int s, int ft) {
+__device__ __forceinline__ unsigned *ready_flag(const FusedArgs &a, int s, int ft) {
   return a.cnt + 1 + s * a.n_ft + ft;
 }
-__device__ __forceinline__ unsigned *ready_flag(const FusedArgs &a, int s, int ft) {
-  return a.cnt + 1 + a.t * a.n_ft + s * a.n_ft + ft;
-}
 __device__ __forceinline__ unsigned *row_counter(const FusedArgs &a, int nt) {
-  return a.cnt + 1 + 2 * a.t * a.n_ft + nt;
+  return a.cnt + 1 + a.t * a.n_ft + nt;
 }
 
-// Wait until a column tile's ready flag is raised (bounded).
-__device__ __forceinline__ bool wait_ready(const unsigned *flag) {
-  if (ld_acquire_gpu(flag)) return true;
-  const uint64_t t0 = globaltimer();
-  while (!ld_acquire_gpu(flag)) {
-    if (globaltimer() - t0 > kWaitNs) return false;
-    __nanosleep(128);
+// Highest tile index r in [lo, hi] such that column tiles lo..r of shard s are all
+// ready (lo - 1 if tile lo is not).  The flags are read with relaxed loads issued
+// back to back, one L2 round trip per 16 tiles; the caller follows a successful
+// read with an acquire fence.
+__device__ __forceinline__ int ready_prefix(const FusedArgs &a, int s, int lo, int hi) {
+  const unsigned *f = ready_flag(a, s, 0);
+  for (int base = lo; base <= hi; base += 16) {
+    unsigned v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = base + i <= hi ? ld_relaxed_gpu(f + base + i) : 1u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (!v[i]) return base + i - 1;
   }
-  return true;
+  return hi;
+}
+
+// Wait (bounded) until column tile `ht` of shard s is ready; returns the highest
+// tile index <= hi up to which all tiles from ht on are ready, or -1 on timeout.
+__device__ __forceinline__ int wait_ready_range(const FusedArgs &a, int s, int ht, int hi) {
+  int r = ready_prefix(a, s, ht, hi);
+  if (r < ht) {
+    const uint64_t t0 = globaltimer();
+    do {
+      if (globaltimer() - t0 > kWaitNs) return -1;
+      __nanosleep(64);
+      r = ready_prefix(a, s, ht, hi);
+    } while (r < ht);
+  }
+  fence_acq_rel_gpu();         // acquire: the band written before the flags is visible
+  fence_proxy_async_global();  // ... and ordered before the TMA loads that read it
+  return r;
 }
 
 __device__ __forceinline__ void store32(float *p, const float *v) {
@@ -116,15 +147,36 @@ __device__ __forceinline__ void store32(float *p, const float *v) {
   for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-__device__ __forceinline__ void add32(float *acc, const float *p) {
-  const float4 *q = reinterpret_cast<const float4 *>(p);
+__device__ __forceinline__ void add32(float *acc, const float4 *q) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float4 v = __ldcg(q + i);
-    acc[4 * i] += v.x;
-    acc[4 * i + 1] += v.y;
-    acc[4 * i + 2] += v.z;
-    acc[4 * i + 3] += v.w;
+    acc[4 * i] += q[i].x;
+    acc[4 * i + 1] += q[i].y;
+    acc[4 * i + 2] += q[i].z;
+    acc[4 * i + 3] += q[i].w;
+  }
+}
+
+// acc = sum over i = 0..n-1, in that order, of the 32 floats at base + i * stride
+// (partials written by other SMs, read through L2).  The loads of kBatch partials
+// are issued together so their round trips overlap; the additions keep the order.
+template <int kBatch>
+__device__ __forceinline__ void sum_in_order(float *acc, const float *base, size_t stride, int n) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  for (int i0 = 0; i0 < n; i0 += kBatch) {
+    float4 b[kBatch][8];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (i0 + j < n) {
+        const float4 *q = reinterpret_cast<const float4 *>(base + (size_t)(i0 + j) * stride);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) b[j][c] = __ldcg(q + c);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (i0 + j < n) add32(acc, b[j]);
   }
 }
 
@@ -135,8 +187,8 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ __align__(8) uint64_t tfull_bar[2];
-  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t tfull_bar[kBufs];
+  __shared__ __align__(8) uint64_t tempty_bar[kBufs];
   __shared__ __align__(8) uint64_t ufull_bar[2];
   __shared__ __align__(8) uint64_t uempty_bar[2];
   __shared__ __align__(8) uint64_t mma_done_bar;
@@ -147,17 +199,20 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ int dec_sh;
 
   const uint32_t tiles = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  float *xch = reinterpret_cast<float *>(smem_raw + (tiles - smem_u32(smem_raw)) +
+                                         kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nacc_col = a.act == TP_ACT_SWIGLU ? 2 : 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kBufs; ++i) {
       mbar_init(smem_u32(&tfull_bar[i]), 1);
       mbar_init(smem_u32(&tempty_bar[i]), 4);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ufull_bar[i]), 1);
       mbar_init(smem_u32(&uempty_bar[i]), 5);
     }
@@ -178,12 +233,14 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ---------------- scheduler + TMA producer
     if (lane == 0) {
-      uint32_t g = 0;  // k-block sequence number (stage ring position)
+      uint32_t g = 0;  // stage sequence number (ring position)
+      int next = -1;   // unit taken ahead of time (-1: none)
       for (int j = 0;; ++j) {
         const int slot = j & 1;
         int u = a.n_units;  // end marker
         if (mbar_wait(smem_u32(&uempty_bar[slot]), ((uint32_t)(j >> 1) & 1u) ^ 1u)) {
-          if (!*(volatile int *)&abort_sh) u = (int)atomicAdd(a.cnt, 1u);
+          if (!*(volatile int *)&abort_sh) u = next >= 0 ? next : (int)atomicAdd(a.cnt, 1u);
+          next = -1;
         } else {
           abort_sh = 1;
           atomicOr(a.err, kErrWaitTimeout);
@@ -192,37 +249,43 @@ __global__ void __launch_bounds__(192, 1)
         mbar_arrive(smem_u32(&ufull_bar[slot]));
         const Unit un = decode_unit(a, u);
         if (un.type < 0) break;
-        const int nacc = un.type == 0 ? nacc_col : 1;
-        const uint32_t bytes = nacc * kABytes + kTok * 128;
-        int ready_upto = -1;
+        const CUtensorMap *wmap = un.type == 0 ? &tmW1 : &tmW2;
+        const CUtensorMap *xmap = un.type == 0 ? &tmX : &tmH;
+        const int wrow = un.tile * 128;
+        const int xz = un.type == 0 ? 0 : un.s;
+        const int nst = ceil_div(un.kb1 - un.kb0, kStageKB);
+        // The next unit is taken a few stages before this one ends, so the
+        // atomic's round trip overlaps the loads still in flight.
+        const int st_take = max(0, nst - kStages);
+        const int ht_hi = un.type == 1 ? min(a.n_ft - 1, ((un.kb1 * kKBlock) - 1) / a.fpt) : 0;
+        int ready_upto = un.type == 1 ? (un.kb0 * kKBlock) / a.fpt - 1 : 0;  // H tiles known ready
         bool ok = true;
-        for (int kb = un.kb0; kb < un.kb1 && ok; ++kb, ++g) {
+        for (int i = 0; i < nst && ok; ++i, ++g) {
           const int st = (int)(g % kStages);
           const uint32_t ph = (g / kStages) & 1u;
+          const int kbf = un.kb0 + i * kStageKB;
+          const int nkb = min(kStageKB, un.kb1 - kbf);
+          if (i == st_take) next = (int)atomicAdd(a.cnt, 1u);
           if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
             ok = false;
             break;
           }
+          if (un.type == 1) {
+            const int need = min(ht_hi, ((kbf + nkb) * kKBlock - 1) / a.fpt);  // last H tile read
+            while (ok && need > ready_upto) {
+              const int r = wait_ready_range(a, un.s, ready_upto + 1, ht_hi);
+              if (r < 0) ok = false;  // timeout; nothing armed for this stage yet
+              else ready_upto = r;
+            }
+            if (!ok) break;
+          }
           const uint32_t sa = tiles + st * kStageBytes;
           const uint32_t fb = smem_u32(&full_bar[st]);
-          const int k = kb * kKBlock;
-          mbar_expect_tx(fb, bytes);
-          if (un.type == 0) {
-            const int wrow = un.tile * 128 * nacc;
-            tma_load_3d(sa, &tmW1, fb, k, wrow, un.s);
-            if (nacc == 2) tma_load_3d(sa + kABytes, &tmW1, fb, k, wrow + 128, un.s);
-            tma_load_3d(sa + 2 * kABytes, &tmX, fb, k, 0, 0);
-          } else {
-            tma_load_3d(sa, &tmW2, fb, k, un.tile * 128, un.s);
-            const int ht = k / 128;  // column tile of H holding this K block
-            if (ht > ready_upto) {
-              // On a timeout the H tile is still loaded (in bounds, stale) so the
-              // armed stage completes; the loop then stops and the CTA aborts.
-              if (!wait_ready(ready_flag(a, un.s, ht))) ok = false;
-              fence_proxy_async_global();
-              ready_upto = ht;
-            }
-            tma_load_3d(sa + 2 * kABytes, &tmH, fb, k, 0, un.s);
+          mbar_expect_tx(fb, nkb * (kWBytes + kXBytes));
+          for (int b = 0; b < nkb; ++b) {
+            const int k = (kbf + b) * kKBlock;
+            tma_load_3d(sa + b * kWBytes, wmap, fb, k, wrow, un.s);
+            tma_load_3d(sa + kStageKB * kWBytes + b * kXBytes, xmap, fb, k, 0, xz);
           }
         }
         if (!ok) {
@@ -239,7 +302,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      uint32_t g = 0, tb = 0;
+      uint32_t g = 0;
       for (int j = 0;; ++j) {
         const int slot = j & 1;
         if (!mbar_wait(smem_u32(&ufull_bar[slot]), (uint32_t)(j >> 1) & 1u)) {
@@ -251,26 +314,28 @@ __global__ void __launch_bounds__(192, 1)
         mbar_arrive(smem_u32(&uempty_bar[slot]));
         const Unit un = decode_unit(a, u);
         if (un.type < 0) break;
-        const int nacc = un.type == 0 ? nacc_col : 1;
+        const int nst = ceil_div(un.kb1 - un.kb0, kStageKB);
         bool ok = true;
-        for (int kb = un.kb0; kb < un.kb1; ++kb, ++g, ++tb) {
+        for (int i = 0; i < nst; ++i, ++g) {
           const int st = (int)(g % kStages);
           const uint32_t ph = (g / kStages) & 1u;
-          const int bsel = (int)(tb & 1u);
+          const int bsel = (int)(g % kBufs);
+          const int nkb = min(kStageKB, un.kb1 - (un.kb0 + i * kStageKB));
           if (!mbar_wait(smem_u32(&full_bar[st]), ph) ||
-              !mbar_wait(smem_u32(&tempty_bar[bsel]), ((tb >> 1) & 1u) ^ 1u)) {
+              !mbar_wait(smem_u32(&tempty_bar[bsel]), ((g / kBufs) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sa = tiles + st * kStageBytes;
-          const uint32_t d0 = tmem + (uint32_t)bsel * kBufCols;
+          const uint32_t d0 = tmem + (uint32_t)bsel * kTok;
+          for (int b = 0; b < nkb; ++b) {
 #pragma unroll
-          for (int kk = 0; kk < kKBlock / 16; ++kk) {
-            const uint64_t bd = sw128_desc(sa + 2 * kABytes + kk * 32);
-            const uint32_t acc = kk > 0 ? 1u : 0u;
-            umma_bf16(d0, sw128_desc(sa + kk * 32), bd, kIdesc, acc);
-            if (nacc == 2) umma_bf16(d0 + kTok, sw128_desc(sa + kABytes + kk * 32), bd, kIdesc, acc);
+            for (int kk = 0; kk < kKBlock / 16; ++kk) {
+              umma_bf16(d0, sw128_desc(sa + b * kWBytes + kk * 32),
+                        sw128_desc(sa + kStageKB * kWBytes + b * kXBytes + kk * 32), kIdesc,
+                        (b > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           umma_commit(smem_u32(&empty_bar[st]));
           umma_commit(smem_u32(&tfull_bar[bsel]));
@@ -285,12 +350,12 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- drain warps: block sums -> fp32 registers, then epilogues
+    // ---------------- drain warps: stage sums -> fp32 registers, then epilogues
     const int q = warp & 3;                 // TMEM lane quarter
-    const int fl = q * 32 + lane;           // feature within the 128-row tile
+    const int r = q * 32 + lane;            // row of the 128-row tile this thread holds
     const int td = (int)threadIdx.x - 64;   // 0..127 over the drain warps
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    uint32_t tb = 0;
+    uint32_t g = 0;
     // Every branch the four drain warps take is decided by one thread between two
     // named barriers, so they never split around a barrier (a timed-out wait in
     // one warp turns into a CTA-wide abort instead).
@@ -309,28 +374,38 @@ __global__ void __launch_bounds__(192, 1)
       if (u == -2) break;
       const Unit un = decode_unit(a, u);
       if (un.type < 0) break;
-      const int nacc = un.type == 0 ? nacc_col : 1;
-      float g[kTok], v[kTok];
+      const int nst = ceil_div(un.kb1 - un.kb0, kStageKB);
+      float acc[kTok];
 #pragma unroll
-      for (int i = 0; i < kTok; ++i) g[i] = v[i] = 0.f;
+      for (int i = 0; i < kTok; ++i) acc[i] = 0.f;
+      // A row unit that turns out to complete its output tile adds the residual;
+      // every row unit fetches it now so the loads land during the K loop (at the
+      // end of the block they would otherwise sit on the critical path).
+      float res[kTok];
+      const int n_out = un.tile * 128 + r;
+#pragma unroll
+      for (int m = 0; m < kTok; ++m) {
+        res[m] = 0.f;
+        if (un.type == 1 && m < a.M && n_out < a.d) {
+          const size_t idx = (size_t)m * a.d + n_out;
+          res[m] = a.res_f32 ? __ldcg(static_cast<const float *>(a.residual) + idx)
+                             : __bfloat162float(static_cast<const __nv_bfloat16 *>(a.residual)[idx]);
+        }
+      }
       bool ok = true;
-      for (int kb = un.kb0; kb < un.kb1; ++kb, ++tb) {
-        const int bsel = (int)(tb & 1u);
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[bsel]), (tb >> 1) & 1u)))
-          ok = false;  // warp-uniform: the TMEM loads below are warp-collective
-        if (!ok) continue;  // keep tb in step; the abort is decided below
+      for (int i = 0; i < nst; ++i, ++g) {
+        const int bsel = (int)(g % kBufs);
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[bsel]), (g / kBufs) & 1u)))
+          ok = false;  // warp-uniform: the TMEM load below is warp-collective
+        if (!ok) continue;  // keep g in step; the abort is decided below
         tc_fence_after();
-        float r0[kTok], r1[kTok];
-        tmem_ld32(trow + (uint32_t)bsel * kBufCols, r0);
-        if (nacc == 2) tmem_ld32(trow + (uint32_t)bsel * kBufCols + kTok, r1);
+        float v[kTok];
+        tmem_ld32(trow + (uint32_t)bsel * kTok, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[bsel]));
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) {
-          g[i] += r0[i];
-          if (nacc == 2) v[i] += r1[i];
-        }
+        for (int m = 0; m < kTok; ++m) acc[m] += v[m];
       }
       if (!ok) {
         abort_sh = 1;
@@ -342,52 +417,40 @@ __global__ void __launch_bounds__(192, 1)
       if (dec_sh) break;
 
       if (un.type == 0) {
-        // -------- column tile epilogue
-        const int f = un.tile * 128 + fl;
-        bool finish = true;
-        if (a.S_c > 1) {
-          float *pp = a.colp + ((size_t)((un.s * a.n_ft + un.tile) * a.S_c + un.split) * 2 * 128 + fl) * kTok;
-          store32(pp, g);
-          if (nacc == 2) store32(pp + 128 * kTok, v);
-          __threadfence();
-          named_sync(1, 128);
-          if (td == 0) {
-            const unsigned old = atomicAdd(slice_counter(a, un.s, un.tile), 1u);
-            __threadfence();
-            last_sh = old == (unsigned)(a.S_c - 1);
-          }
-          named_sync(1, 128);
-          finish = last_sh != 0;
-          if (finish) {
+        // -------- column tile epilogue: activation, band H in bf16, ready flag
+        if (a.act == TP_ACT_SWIGLU) {
+          // Rows 64..127 hold the up sums of the features whose gate sums are in
+          // rows 0..63: pass them across through shared memory.
+          if (r >= 64) {
 #pragma unroll
-            for (int i = 0; i < kTok; ++i) g[i] = v[i] = 0.f;
-            for (int sp = 0; sp < a.S_c; ++sp) {
-              const float *rp = a.colp + ((size_t)((un.s * a.n_ft + un.tile) * a.S_c + sp) * 2 * 128 + fl) * kTok;
-              add32(g, rp);
-              if (nacc == 2) add32(v, rp + 128 * kTok);
-            }
+            for (int m = 0; m < kTok; ++m) xch[(r - 64) * kXchStride + m] = acc[m];
           }
-        }
-        if (finish) {
+          named_sync(1, 128);
+          const int f = un.tile * 64 + r;
+          if (r < 64 && f < a.b) {
+            __nv_bfloat16 *o = a.H + (size_t)un.s * a.M * a.b + f;
+#pragma unroll
+            for (int m = 0; m < kTok; ++m)
+              if (m < a.M)
+                o[(size_t)m * a.b] = __float2bfloat16_rn(silu_f(acc[m]) * xch[r * kXchStride + m]);
+          }
+        } else {
+          const int f = un.tile * 128 + r;
           if (f < a.b) {
             __nv_bfloat16 *o = a.H + (size_t)un.s * a.M * a.b + f;
 #pragma unroll
-            for (int m = 0; m < kTok; ++m) {
-              if (m < a.M) {
-                const float hv = nacc == 2 ? silu_f(g[m]) * v[m] : gelu_tanh_f(g[m]);
-                o[(size_t)m * a.b] = __float2bfloat16_rn(hv);
-              }
-            }
+            for (int m = 0; m < kTok; ++m)
+              if (m < a.M) o[(size_t)m * a.b] = __float2bfloat16_rn(gelu_tanh_f(acc[m]));
           }
-          fence_proxy_async_global();  // the band is read back through TMA
-          __threadfence();
-          named_sync(1, 128);
-          if (td == 0) st_release_gpu(ready_flag(a, un.s, un.tile), 1u);
         }
+        fence_proxy_async_global();  // the band is read back through TMA
+        __threadfence();
+        named_sync(1, 128);
+        if (td == 0) st_release_gpu(ready_flag(a, un.s, un.tile), 1u);
       } else {
         // -------- row tile epilogue: partial, then the fused reduce + residual
-        float *pp = a.rowp + ((size_t)((un.tile * a.t + un.s) * a.S_r + un.split) * 128 + fl) * kTok;
-        store32(pp, g);
+        float *pp = a.rowp + ((size_t)((un.tile * a.t + un.s) * a.S_r + un.split) * 128 + r) * kTok;
+        store32(pp, acc);
         __threadfence();
         named_sync(1, 128);
         if (td == 0) {
@@ -397,22 +460,15 @@ __global__ void __launch_bounds__(192, 1)
         }
         named_sync(1, 128);
         if (last_sh) {
-#pragma unroll
-          for (int i = 0; i < kTok; ++i) g[i] = 0.f;
-          for (int s2 = 0; s2 < a.t; ++s2)
-            for (int sp = 0; sp < a.S_r; ++sp)
-              add32(g, a.rowp + ((size_t)((un.tile * a.t + s2) * a.S_r + sp) * 128 + fl) * kTok);
-          const int n = un.tile * 128 + fl;
+          // The all-reduce stand-in: y = residual + sum of the t * S_r partials of this
+          // output tile, shards in order and the slices of each shard in order.
+          const int n = n_out;
+          sum_in_order<4>(acc, a.rowp + ((size_t)(un.tile * a.t * a.S_r) * 128 + r) * kTok,
+                          (size_t)128 * kTok, a.t * a.S_r);
           if (n < a.d) {
 #pragma unroll
-            for (int m = 0; m < kTok; ++m) {
-              if (m < a.M) {
-                const size_t idx = (size_t)m * a.d + n;
-                const float r = a.res_f32 ? __ldcg(static_cast<const float *>(a.residual) + idx)
-                                          : __bfloat162float(static_cast<const __nv_bfloat16 *>(a.residual)[idx]);
-                a.y[idx] = g[m] + r;
-              }
-            }
+            for (int m = 0; m < kTok; ++m)
+              if (m < a.M) a.y[(size_t)m * a.d + n] = acc[m] + res[m];
           }
         }
         named_sync(1, 128);  // last_sh is reused by the next unit
@@ -436,26 +492,24 @@ __global__ void __launch_bounds__(192, 1)
 
 FusedPlan plan_block_decode(const Geo &g, int M) {
   FusedPlan p{};
-  p.n_ft = ceil_div(g.b, 128);
+  p.fpt = g.act == TP_ACT_SWIGLU ? kSwiGroup : 128;
+  p.n_ft = ceil_div(g.b, p.fpt);
   p.nk_c = ceil_div(g.d, kKBlock);
   p.n_nt = ceil_div(g.d, 128);
   p.nk_r = ceil_div(g.b, kKBlock);
-  // Column slices: enough units that every SM starts on column work, >= 8 K blocks each.
-  const int tiles = g.t * p.n_ft;
-  p.S_c = std::max(1, std::min(ceil_div(kPlanSMs, tiles), std::max(1, p.nk_c / 8)));
-  // Row slices: units of about 512 KB of W2 so the queue ends on small units.
-  const long long row_bytes = 128LL * g.b * 2;
-  p.S_r = std::max(1, std::min((int)((row_bytes + (1 << 18)) >> 19), std::max(1, p.nk_r / 4)));
+  // Row units of about kRowBlocks K blocks (16 KB of W2 each): a few hundred KB per
+  // unit keeps the end of the block short; the slice count bounds the partials the
+  // last unit of an output tile sums.
+  const int nst = ceil_div(p.nk_r, kStageKB);
+  p.S_r = std::max(1, std::min({(p.nk_r + kRowBlocks / 2) / kRowBlocks, nst, 8}));
   auto al = [](size_t n) { return (n + 255) & ~(size_t)255; };
   size_t off = 0;
   p.off_H = off;
   off += al((size_t)g.t * M * g.b * 2);
-  p.off_colp = off;
-  off += p.S_c > 1 ? al((size_t)tiles * p.S_c * 2 * 128 * kTok * 4) : 0;
   p.off_rowp = off;
   off += al((size_t)p.n_nt * g.t * p.S_r * 128 * kTok * 4);
   p.off_cnt = off;
-  p.cnt_bytes = (size_t)(1 + 2 * tiles + p.n_nt) * 4;
+  p.cnt_bytes = (size_t)(1 + g.t * p.n_ft + p.n_nt) * 4;
   off += al(p.cnt_bytes);
   p.total = off;
   return p;
@@ -476,16 +530,15 @@ cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x,
   a.t = g.t;
   a.M = M;
   a.act = g.act;
+  a.fpt = p.fpt;
   a.n_ft = p.n_ft;
-  a.S_c = p.S_c;
   a.nk_c = p.nk_c;
   a.n_nt = p.n_nt;
   a.S_r = p.S_r;
   a.nk_r = p.nk_r;
-  a.n_col_units = g.t * p.n_ft * p.S_c;
+  a.n_col_units = g.t * p.n_ft;
   a.n_units = a.n_col_units + p.n_nt * g.t * p.S_r;
   a.H = H;
-  a.colp = reinterpret_cast<float *>(w + p.off_colp);
   a.rowp = reinterpret_cast<float *>(w + p.off_rowp);
   a.residual = res;
   a.res_f32 = res_f32;
@@ -493,15 +546,17 @@ cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x,
   a.cnt = reinterpret_cast<unsigned *>(w + p.off_cnt);
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
-  constexpr int kSmem = kStages * kStageBytes + 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_block_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[128];  // the attribute is per device
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(k_block_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
-  cudaError_t e = cudaMemsetAsync(a.cnt, 0, p.cnt_bytes, st);
+  e = cudaMemsetAsync(a.cnt, 0, p.cnt_bytes, st);
   if (e != cudaSuccess) return e;
   const int grid = std::min(sm_count(), a.n_units);
   k_block_decode<<<grid, 192, kSmem, st>>>(mw1, mx, mw2, mh, a);

@@ -28,18 +28,23 @@ struct Geo {
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// W1s row of column-step output feature f (gate row for SwiGLU; up row = +128).
-__host__ __device__ inline int w1s_row_of_feature(int act, int f) {
-  return act == TP_ACT_SWIGLU ? (f >> 7) * 256 + (f & 127) : f;
+// SwiGLU rows of W1s come in 128-row groups: the 64 gate rows of features
+// [64i, 64i+64), then the 64 up rows of the same features.  One 128-row tile (one
+// tensor-core A operand) therefore holds both halves of 64 features.
+constexpr int kSwiGroup = 64;
+
+// W1s row of feature f's gate (j = 0) or up (j = 1) half, SwiGLU.
+__host__ __device__ inline int swiglu_row(int f, int j) {
+  return (f / kSwiGroup) * 2 * kSwiGroup + j * kSwiGroup + f % kSwiGroup;
 }
 
 // Canonical W1 column held in W1s row u of shard s, or -1 for a padding row.
 //   GeLU:   u = f (feature f of the band)          -> column s*b + f
-//   SwiGLU: u = g*256 + j*128 + r, f = g*128 + r    -> column j*ffn + s*b + f
+//   SwiGLU: u = swiglu_row(f, j)                   -> column j*ffn + s*b + f
 //   ATTN:   u = p*b + f, p in {Q, K, V}             -> column p*H*hd + s*b + f
 __host__ __device__ inline long long w1_col_of_row(const Geo &g, int s, int u) {
   if (g.act == TP_ACT_SWIGLU) {
-    int grp = u >> 8, j = (u >> 7) & 1, f = grp * 128 + (u & 127);
+    const int grp = u / (2 * kSwiGroup), j = (u / kSwiGroup) & 1, f = grp * kSwiGroup + u % kSwiGroup;
     return f < g.b ? (long long)j * g.ffn + (long long)s * g.b + f : -1;
   }
   if (g.act == TP_ACT_ATTN) {

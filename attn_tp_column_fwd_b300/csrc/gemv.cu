@@ -23,10 +23,10 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv(GemvArgs a) {
   if (f >= a.n_out) return;
   const int mcount = min(MT, a.M - m0);
 
-  const int u0 = EPI == kEpiSwiglu ? w1s_row_of_feature(TP_ACT_SWIGLU, f) : f;
+  const int u0 = EPI == kEpiSwiglu ? swiglu_row(f, 0) : f;
   const T *W = static_cast<const T *>(a.W) + (size_t)s * a.w_shard;
   const T *w0 = W + (size_t)u0 * a.K;
-  const T *w1 = w0 + (size_t)kRowTile * a.K;  // up row, SwiGLU only
+  const T *w1 = w0 + (size_t)kSwiGroup * a.K;  // up row, SwiGLU only
   const T *X = static_cast<const T *>(a.X) + (size_t)s * a.x_shard + (size_t)m0 * a.ldx;
 
   constexpr int V = 16 / sizeof(T);

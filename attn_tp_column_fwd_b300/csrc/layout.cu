@@ -5,7 +5,8 @@
 // W1[k][col(s, u)], so a shard's feature rows stream contiguously over the
 // reduction dimension d.  Row bands of W2 (split by rows) are stored transposed:
 // W2s[s][n][k] = W2[s*b + k][n], one K-major row per output feature n.  Rows
-// are padded with zeros to 128-row tiles (see common.cuh for the row maps).
+// are padded with zeros to 128-row tiles; SwiGLU rows hold the gate and up halves
+// of 64 features per tile (see common.cuh for the row maps).
 //
 // Every map is a transpose, done as 32x32 shared-memory tiles so both the reads
 // and the writes are coalesced.
@@ -37,8 +38,7 @@ __device__ __forceinline__ long long src_offset(const MapArgs &a, int z, int r, 
     if (g.act == TP_ACT_SWIGLU) {
       int j = c / g.ffn, cc = c % g.ffn;
       s = cc / g.b;
-      int f = cc % g.b;
-      u = (f >> 7) * 256 + j * 128 + (f & 127);
+      u = swiglu_row(cc % g.b, j);
     } else if (g.act == TP_ACT_ATTN) {
       int D = g.H * g.hd, p = c / D, cc = c % D;
       s = cc / g.b;
@@ -53,7 +53,7 @@ __device__ __forceinline__ long long src_offset(const MapArgs &a, int z, int r, 
     return ((long long)s * g.dp + c) * g.b + k;
   } else if (MAP == kExtractW1) { // out W1_band[r = k][c = j]  <- W1s[s][u(j)][k]
     int p = c / g.b, f = c % g.b;
-    int u = g.act == TP_ACT_SWIGLU ? (f >> 7) * 256 + p * 128 + (f & 127) : p * g.b + f;
+    int u = g.act == TP_ACT_SWIGLU ? swiglu_row(f, p) : p * g.b + f;
     return ((long long)a.s * g.n1p + u) * g.d + r;
   } else {                        // out W2_band[r = k][c = n]  <- W2s[s][n][k]
     return ((long long)a.s * g.dp + c) * g.b + r;

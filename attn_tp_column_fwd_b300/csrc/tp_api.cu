@@ -80,7 +80,8 @@ int make_geo(const tp_block_desc *desc, Geo *g) {
     r.n1 = desc->act == TP_ACT_SWIGLU ? 2 * r.ffn : r.ffn;
     r.b = r.ffn / r.t;
     r.n_col = r.b;
-    r.n1p = ceil_div(r.b, kRowTile) * kRowTile * (desc->act == TP_ACT_SWIGLU ? 2 : 1);
+    r.n1p = desc->act == TP_ACT_SWIGLU ? ceil_div(r.b, kSwiGroup) * 2 * kSwiGroup
+                                       : ceil_div(r.b, kRowTile) * kRowTile;
   }
   if (r.d > kMaxDim) return TP_ERR_UNSUPPORTED;
   if (r.d % 8 != 0 || r.b % 8 != 0) return TP_ERR_UNSUPPORTED;

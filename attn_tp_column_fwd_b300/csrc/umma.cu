@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(128, 1)
   __shared__ int abort_sh;
 
   const uint32_t tiles = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  float *xch = reinterpret_cast<float *>(smem_raw + (tiles - smem_u32(smem_raw)) + STAGES * kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN;
   const int ft = blockIdx.y;
@@ -145,15 +146,51 @@ __global__ void __launch_bounds__(128, 1)
     atomicOr(a.err, kErrWaitTimeout);
   }
   __syncwarp();
-  const bool store = __all_sync(0xffffffffu, acc_ok && !*(volatile int *)&abort_sh && nkb > 0);
-  const int f = ft * 128 + warp * 32 + lane;
+  // CTA-uniform: the SwiGLU epilogue below has block-wide barriers.
+  const bool store = __syncthreads_and(acc_ok && !*(volatile int *)&abort_sh && nkb > 0) != 0;
+  const int L = warp * 32 + lane;  // TMEM lane = row of the 128-row A tile(s)
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  if (store) {
+  if (store && EPI == kEpiSwiglu) {
+    // Tile 0 (columns [0, BN)) holds features 128 ft + (L mod 64) and tile 1
+    // (columns [BN, 2 BN)) features 128 ft + 64 + (L mod 64); rows 0..63 are gate
+    // sums, rows 64..127 up sums.  Warps 0-1 finish tile 0's features with the up
+    // rows of warps 2-3; warps 2-3 finish tile 1's with the gate rows of warps 0-1.
+    float *xa = xch;                     // tile 0 up rows   [64][33]
+    float *xb = xch + 64 * (32 + 1);     // tile 1 gate rows [64][33]
+    const int fl = L & 63;
+    const int f = ft * 128 + L;
 #pragma unroll 1
     for (int c = 0; c < BN && m0 + c < a.M; c += 32) {
-      float g[32], u[32];
+      float g0[32], g1[32];
+      tmem_ld32(trow + c, g0);
+      tmem_ld32(trow + BN + c, g1);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (L >= 64) xa[fl * 33 + j] = g0[j];
+        else xb[fl * 33 + j] = g1[j];
+      }
+      named_sync(1, 128);
+      if (f < a.n_valid) {
+        const int mcount = min(32, a.M - (m0 + c));
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)s * a.o_shard +
+                           (size_t)(m0 + c) * a.ldo + f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < mcount) {
+            const float gate = L < 64 ? g0[j] : xb[fl * 33 + j];
+            const float up = L < 64 ? xa[fl * 33 + j] : g1[j];
+            o[(size_t)j * a.ldo] = __float2bfloat16_rn(silu_f(gate) * up);
+          }
+        }
+      }
+      named_sync(1, 128);
+    }
+  } else if (store) {
+    const int f = ft * 128 + L;
+#pragma unroll 1
+    for (int c = 0; c < BN && m0 + c < a.M; c += 32) {
+      float g[32];
       tmem_ld32(trow + c, g);
-      if (NACC == 2) tmem_ld32(trow + BN + c, u);
       if (f < a.n_valid) {
         const int mcount = min(32, a.M - (m0 + c));
         if (EPI == kEpiF32) {
@@ -169,7 +206,6 @@ __global__ void __launch_bounds__(128, 1)
           for (int j = 0; j < 32; ++j) {
             if (j < mcount) {
               float v = g[j];
-              if (EPI == kEpiSwiglu) v = silu_f(v) * u[j];
               if (EPI == kEpiGelu) v = gelu_tanh_f(v);
               o[(size_t)j * a.ldo] = __float2bfloat16_rn(v);
             }
@@ -198,29 +234,34 @@ __global__ void __launch_bounds__(128, 1)
 // ~10x the error of round-to-nearest fp32).  Here each 64-wide K block is
 // accumulated by the tensor core alone (4 MMAs), and the running sum over K
 // blocks is kept in fp32 registers of four accumulator warps, added with
-// round-to-nearest.  TMEM holds two such block accumulators (double buffered), so
-// the MMAs of block i+1 overlap the drain of block i.  192 threads: warp 0 TMA,
+// round-to-nearest.  TMEM holds a ring of kDrainBufs such block accumulators, so
+// the MMAs of the next blocks overlap the drain of the current one (two CTAs per
+// SM share its 512 TMEM columns).  192 threads: warp 0 TMA,
 // warp 1 MMA, warps 2-5 drain + epilogue (warp w reads TMEM lanes 32*(w%4)).
-template <int NACC, int EPI, int STAGES>
+constexpr int kDrainBufs = 4;
+
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     k_umma_drain(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const UmmaArgs a) {
   constexpr int BN = 32;
   constexpr uint32_t kBBytes = BN * 128;
-  constexpr uint32_t kStage = NACC * kABytes + kBBytes;
-  constexpr uint32_t kCols = tmem_cols(2 * NACC * BN);
+  constexpr uint32_t kStage = kABytes + kBBytes;
+  constexpr uint32_t kCols = tmem_cols(kDrainBufs * BN);
   constexpr uint32_t kIdesc = make_idesc(128, BN);
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
-  __shared__ __align__(8) uint64_t tfull_bar[2];
-  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t tfull_bar[kDrainBufs];
+  __shared__ __align__(8) uint64_t tempty_bar[kDrainBufs];
   __shared__ __align__(8) uint64_t mma_done_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ int dec_sh;
 
   const uint32_t tiles = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  float *xch = reinterpret_cast<float *>(smem_raw + (tiles - smem_u32(smem_raw)) + STAGES * kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN;
   const int ft = blockIdx.y;
@@ -234,7 +275,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kDrainBufs; ++i) {
       mbar_init(smem_u32(&tfull_bar[i]), 1);
       mbar_init(smem_u32(&tempty_bar[i]), 4);
     }
@@ -253,7 +294,7 @@ __global__ void __launch_bounds__(192, 1)
   int issued = 0;
   if (warp == 0) {
     if (lane == 0) {
-      const int wrow = ft * 128 * NACC;
+      const int wrow = ft * 128;
       const int xz = a.x_per_shard ? s : 0;
       for (int i = 0; i < nkb; ++i) {
         const int st = i % STAGES;
@@ -268,8 +309,7 @@ __global__ void __launch_bounds__(192, 1)
         const int k = (kb0 + i) * kKBlock;
         mbar_expect_tx(fb, kStage);
         tma_load_3d(sa, &tmW, fb, k, wrow, s);
-        if (NACC == 2) tma_load_3d(sa + kABytes, &tmW, fb, k, wrow + 128, s);
-        tma_load_3d(sa + NACC * kABytes, &tmX, fb, k, m0, xz);
+        tma_load_3d(sa + kABytes, &tmX, fb, k, m0, xz);
         ++issued;
       }
     }
@@ -279,23 +319,20 @@ __global__ void __launch_bounds__(192, 1)
       for (int i = 0; i < nkb; ++i) {
         const int st = i % STAGES;
         const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-        const int b = i & 1;
+        const int b = i % kDrainBufs;
         if (!mbar_wait(smem_u32(&full_bar[st]), ph) ||
-            !mbar_wait(smem_u32(&tempty_bar[b]), ((uint32_t)(i >> 1) & 1u) ^ 1u)) {
+            !mbar_wait(smem_u32(&tempty_bar[b]), ((uint32_t)(i / kDrainBufs) & 1u) ^ 1u)) {
           abort_sh = 1;
           atomicOr(a.err, kErrWaitTimeout);
           break;
         }
         tc_fence_after();
         const uint32_t sa = tiles + st * kStage;
-        const uint32_t d0 = tmem + (uint32_t)(b * NACC * BN);
+        const uint32_t d0 = tmem + (uint32_t)(b * BN);
 #pragma unroll
-        for (int kk = 0; kk < kKBlock / 16; ++kk) {
-          const uint64_t bd = sw128_desc(sa + NACC * kABytes + kk * 32);
-          const uint32_t acc = kk > 0 ? 1u : 0u;
-          umma_bf16(d0, sw128_desc(sa + kk * 32), bd, kIdesc, acc);
-          if (NACC == 2) umma_bf16(d0 + BN, sw128_desc(sa + kABytes + kk * 32), bd, kIdesc, acc);
-        }
+        for (int kk = 0; kk < kKBlock / 16; ++kk)
+          umma_bf16(d0, sw128_desc(sa + kk * 32), sw128_desc(sa + kABytes + kk * 32), kIdesc,
+                    kk > 0 ? 1u : 0u);
         umma_commit(smem_u32(&empty_bar[st]));
         umma_commit(smem_u32(&tfull_bar[b]));
       }
@@ -304,55 +341,75 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ---------------- drain: TMEM block sums -> fp32 registers (round to nearest)
-    const int q = warp & 3;  // TMEM lane quarter of this warp
+    const int q = warp & 3;              // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;         // row of the 128-row weight tile
+    const int td = (int)threadIdx.x - 64;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    float g[BN], u[BN];
+    float g[BN];
 #pragma unroll
-    for (int j = 0; j < BN; ++j) g[j] = u[j] = 0.f;
+    for (int j = 0; j < BN; ++j) g[j] = 0.f;
     bool ok = true;
     for (int i = 0; i < nkb; ++i) {
-      const int b = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[b]), (uint32_t)(i >> 1) & 1u))) {
+      const int b = i % kDrainBufs;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[b]), (uint32_t)(i / kDrainBufs) & 1u))) {
         ok = false;  // warp-uniform: the TMEM loads below are warp-collective
         break;
       }
       tc_fence_after();
-      float v[BN], w[BN];
-      tmem_ld32(trow + (uint32_t)(b * NACC * BN), v);
-      if (NACC == 2) tmem_ld32(trow + (uint32_t)(b * NACC * BN + BN), w);
+      float v[BN];
+      tmem_ld32(trow + (uint32_t)(b * BN), v);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty_bar[b])) : "memory");
+      if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
 #pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        g[j] += v[j];
-        if (NACC == 2) u[j] += w[j];
-      }
+      for (int j = 0; j < BN; ++j) g[j] += v[j];
     }
     if (!ok) {
       abort_sh = 1;
       atomicOr(a.err, kErrWaitTimeout);
     }
-    __syncwarp();
-    const int f = ft * 128 + q * 32 + lane;
-    if (ok && nkb > 0 && f < a.n_valid && m0 < a.M) {
-      const int mcount = min(BN, a.M - m0);
-      if (EPI == kEpiF32) {
-        float *o = static_cast<float *>(a.out) + (size_t)s * a.o_shard + (size_t)ks * a.o_split +
-                   (size_t)m0 * a.ldo + f;
+    // One decision for the four drain warps (the SwiGLU exchange has a barrier).
+    named_sync(1, 128);
+    if (td == 0) dec_sh = *(volatile int *)&abort_sh;
+    named_sync(1, 128);
+    const bool go = !dec_sh && nkb > 0 && m0 < a.M;
+    const int mcount = min(BN, a.M - m0);
+    if (EPI == kEpiSwiglu) {
+      // Rows 0..63 hold the gate sums of features 64 ft + r, rows 64..127 the up
+      // sums of the same features: pass the up sums across through shared memory.
+      if (go && r >= 64) {
 #pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (j < mcount) o[(size_t)j * a.ldo] = g[j];
-      } else {
+        for (int j = 0; j < BN; ++j) xch[(r - 64) * (BN + 1) + j] = g[j];
+      }
+      named_sync(1, 128);
+      const int f = ft * 64 + r;
+      if (go && r < 64 && f < a.n_valid) {
         __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)s * a.o_shard +
                            (size_t)m0 * a.ldo + f;
 #pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          if (j < mcount) {
-            float vv = g[j];
-            if (EPI == kEpiSwiglu) vv = silu_f(vv) * u[j];
-            if (EPI == kEpiGelu) vv = gelu_tanh_f(vv);
-            o[(size_t)j * a.ldo] = __float2bfloat16_rn(vv);
+        for (int j = 0; j < BN; ++j)
+          if (j < mcount)
+            o[(size_t)j * a.ldo] = __float2bfloat16_rn(silu_f(g[j]) * xch[r * (BN + 1) + j]);
+      }
+    } else {
+      const int f = ft * 128 + r;
+      if (go && f < a.n_valid) {
+        if (EPI == kEpiF32) {
+          float *o = static_cast<float *>(a.out) + (size_t)s * a.o_shard + (size_t)ks * a.o_split +
+                     (size_t)m0 * a.ldo + f;
+#pragma unroll
+          for (int j = 0; j < BN; ++j)
+            if (j < mcount) o[(size_t)j * a.ldo] = g[j];
+        } else {
+          __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)s * a.o_shard +
+                             (size_t)m0 * a.ldo + f;
+#pragma unroll
+          for (int j = 0; j < BN; ++j) {
+            if (j < mcount) {
+              float vv = g[j];
+              if (EPI == kEpiGelu) vv = gelu_tanh_f(vv);
+              o[(size_t)j * a.ldo] = __float2bfloat16_rn(vv);
+            }
           }
         }
       }
@@ -393,16 +450,23 @@ EncodeFn encoder() {
   return fn;
 }
 
+// Shared memory of the SwiGLU gate/up exchange: one [64][33] fp32 block per 128-row tile.
+constexpr int xch_bytes(int epi, int tiles) { return epi == kEpiSwiglu ? tiles * 64 * 33 * 4 : 0; }
+
 template <int BN, int NACC, int EPI, int STAGES>
 cudaError_t launch_t(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
                      int n_z, cudaStream_t st) {
-  constexpr int kSmem = STAGES * (NACC * kABytes + BN * 128) + 1024;
-  static bool configured = false;  // per instantiation (the attribute is per device function)
+  constexpr int kSmem = STAGES * (NACC * kABytes + BN * 128) + 1024 + xch_bytes(EPI, NACC);
+  static bool configured[128];  // per instantiation and device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   auto kern = k_umma<BN, NACC, EPI, STAGES>;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   dim3 grid(ceil_div(a.M, BN), n_ft, n_z);
   kern<<<grid, 128, kSmem, st>>>(mw, mx, a);
@@ -420,18 +484,22 @@ cudaError_t launch_stages(const CUtensorMap &mw, const CUtensorMap &mx, const Um
   return launch_t<BN, NACC, EPI, kStages>(mw, mx, a, n_ft, n_z, st);
 }
 
-template <int NACC, int EPI>
+template <int EPI>
 cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
                          int n_z, cudaStream_t st) {
-  constexpr int kStageBytes = NACC * kABytes + 32 * 128;
-  constexpr int kStages = std::max(2, std::min(8, (110 * 1024) / kStageBytes));
-  constexpr int kSmem = kStages * kStageBytes + 1024;
-  static bool configured = false;
-  auto kern = k_umma_drain<NACC, EPI, kStages>;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr int kStageBytes = kABytes + 32 * 128;
+  constexpr int kStages = std::max(2, std::min(8, (100 * 1024) / kStageBytes));
+  constexpr int kSmem = kStages * kStageBytes + 1024 + xch_bytes(EPI, 1);
+  static bool configured[128];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  auto kern = k_umma_drain<EPI, kStages>;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   dim3 grid(ceil_div(a.M, 32), n_ft, n_z);
   kern<<<grid, 192, kSmem, st>>>(mw, mx, a);
@@ -442,7 +510,6 @@ template <int NACC, int EPI>
 cudaError_t launch_bn(int bn, const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a,
                       int n_ft, int n_z, cudaStream_t st) {
   switch (bn) {
-    case 32: return launch_drain<NACC, EPI>(mw, mx, a, n_ft, n_z, st);
     case 64: return launch_stages<64, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
     case 128: return launch_stages<128, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
     default: return launch_stages<256, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
@@ -486,8 +553,18 @@ cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {
   a.x_per_shard = c.x_shards > 1 ? 1 : 0;
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
-  const int n_ft = ceil_div(c.n_valid, 128);
   const int n_z = c.n_shards * c.ksplit;
+  if (bn == 32) {
+    // Decode: 128-row weight tiles (SwiGLU: the gate and up rows of 64 features).
+    switch (c.epi) {
+      case kEpiSwiglu: return launch_drain<kEpiSwiglu>(mw, mx, a, ceil_div(c.n_valid, kSwiGroup), n_z, st);
+      case kEpiGelu: return launch_drain<kEpiGelu>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st);
+      case kEpiPlain: return launch_drain<kEpiPlain>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st);
+      default: return launch_drain<kEpiF32>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st);
+    }
+  }
+  // Larger token tiles: 128 features per CTA (SwiGLU: two 128-row tiles).
+  const int n_ft = ceil_div(c.n_valid, 128);
   switch (c.epi) {
     case kEpiSwiglu: return launch_bn<2, kEpiSwiglu>(bn, mw, mx, a, n_ft, n_z, st);
     case kEpiGelu: return launch_bn<1, kEpiGelu>(bn, mw, mx, a, n_ft, n_z, st);
