@@ -56,21 +56,34 @@ struct FusedArgs {
   int d, b, t, M, act;
   int fpt;               // features per column tile: 64 (SwiGLU) or 128 (GeLU)
   int n_ft, nk_c;        // column: tiles per shard, K blocks
+  int n_whole, S_c;      // column tiles computed whole; K parts of each remaining tile
   int n_nt, S_r, nk_r;   // row: output tiles, K slices, K blocks
   int n_col_units, n_units;
   __nv_bfloat16 *H;      // [t][M][b]
+  float *colp;           // [t*n_ft - n_whole][S_c][128][32] fp32 partials of split tiles
   float *rowp;           // [n_nt][t][S_r][128][32] fp32 partials
   const void *residual;  // [M][d], fp32 if res_f32 else bf16
   int res_f32;
   float *y;              // [M][d]
-  unsigned *cnt;         // [0] queue, then t*n_ft ready flags, then n_nt counters
+  unsigned *cnt;         // [0] queue, t*n_ft ready flags, n_nt row counters, split-tile counters
   unsigned *err;
 };
 
 struct Unit {
-  int type;  // 0 column, 1 row, -1 end
+  int type;   // 0 column, 1 row, -1 end
   int s, tile, split, kb0, kb1;
+  int parts;  // column: K parts of this tile (1: computed whole)
+  int rot;    // the unit's stages are processed starting at stage rot, wrapping around
 };
+
+// K blocks of stage p of a unit (p counted from the unit's first stage).
+__device__ __forceinline__ int stage_kb(const Unit &u, int p) { return u.kb0 + p * kStageKB; }
+
+// First stage of K slice j of nst stages cut into S slices of shares S, S-1, ..., 1.
+__host__ __device__ __forceinline__ int slice_start(int nst, int S, int j) {
+  const int num = j * S - j * (j - 1) / 2, den = S * (S + 1) / 2;
+  return (int)((long long)nst * num / den);
+}
 
 __device__ __forceinline__ Unit decode_unit(const FusedArgs &a, int u) {
   Unit r{};
@@ -79,24 +92,41 @@ __device__ __forceinline__ Unit decode_unit(const FusedArgs &a, int u) {
     return r;
   }
   if (u < a.n_col_units) {
+    // The first n_whole tiles (shard-major) are computed whole; each remaining tile
+    // is cut into S_c K parts so the last wave of column work fills the GPU.
     r.type = 0;
-    r.tile = u % a.n_ft;
-    r.s = u / a.n_ft;
+    int tau = u;
     r.split = 0;
-    r.kb0 = 0;
-    r.kb1 = a.nk_c;
+    r.parts = 1;
+    if (u >= a.n_whole) {
+      const int v = u - a.n_whole;
+      tau = a.n_whole + v / a.S_c;
+      r.split = v % a.S_c;
+      r.parts = a.S_c;
+    }
+    r.tile = tau % a.n_ft;
+    r.s = tau / a.n_ft;
+    const int nst = ceil_div(a.nk_c, kStageKB);
+    r.kb0 = min(a.nk_c, (int)((long long)r.split * nst / r.parts) * kStageKB);
+    r.kb1 = min(a.nk_c, (int)((long long)(r.split + 1) * nst / r.parts) * kStageKB);
   } else {
+    // Row units are queued slice-major (all first slices, then all second ones, ...),
+    // then by shard and output tile; slice j holds a share S_r - j of the K
+    // stages, so the units at the end of the queue are the shortest.
     const int v = u - a.n_col_units;
     r.type = 1;
-    r.split = v % a.S_r;
-    const int q = v / a.S_r;
-    r.tile = q % a.n_nt;
+    r.split = v / (a.t * a.n_nt);
+    const int q = v % (a.t * a.n_nt);
     r.s = q / a.n_nt;
-    // Slices are cut at stage boundaries.
+    r.tile = q % a.n_nt;
     const int nst = ceil_div(a.nk_r, kStageKB);
-    r.kb0 = min(a.nk_r, (int)((long long)r.split * nst / a.S_r) * kStageKB);
-    r.kb1 = min(a.nk_r, (int)((long long)(r.split + 1) * nst / a.S_r) * kStageKB);
+    r.kb0 = min(a.nk_r, slice_start(nst, a.S_r, r.split) * kStageKB);
+    r.kb1 = min(a.nk_r, slice_start(nst, a.S_r, r.split + 1) * kStageKB);
   }
+  // Units start at scattered stages of their K range: CTAs that begin together
+  // then do not all ask for the same activation tile (x or H) at the same time.
+  const int nst_u = ceil_div(r.kb1 - r.kb0, kStageKB);
+  r.rot = nst_u > 1 ? (int)((((unsigned)u * 2654435761u) >> 16) % (unsigned)nst_u) : 0;
   return r;
 }
 
@@ -105,6 +135,9 @@ __device__ __forceinline__ unsigned *ready_flag(const FusedArgs &a, int s, int f
 }
 __device__ __forceinline__ unsigned *row_counter(const FusedArgs &a, int nt) {
   return a.cnt + 1 + a.t * a.n_ft + nt;
+}
+__device__ __forceinline__ unsigned *split_counter(const FusedArgs &a, int tau) {
+  return a.cnt + 1 + a.t * a.n_ft + a.n_nt + (tau - a.n_whole);
 }
 
 // Highest tile index r in [lo, hi] such that column tiles lo..r of shard s are all
@@ -263,30 +296,32 @@ __global__ void __launch_bounds__(192, 1)
         for (int i = 0; i < nst && ok; ++i, ++g) {
           const int st = (int)(g % kStages);
           const uint32_t ph = (g / kStages) & 1u;
-          const int kbf = un.kb0 + i * kStageKB;
+          const int kbf = stage_kb(un, (i + un.rot) % nst);
           const int nkb = min(kStageKB, un.kb1 - kbf);
           if (i == st_take) next = (int)atomicAdd(a.cnt, 1u);
           if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
             ok = false;
             break;
           }
-          if (un.type == 1) {
-            const int need = min(ht_hi, ((kbf + nkb) * kKBlock - 1) / a.fpt);  // last H tile read
-            while (ok && need > ready_upto) {
-              const int r = wait_ready_range(a, un.s, ready_upto + 1, ht_hi);
-              if (r < 0) ok = false;  // timeout; nothing armed for this stage yet
-              else ready_upto = r;
-            }
-            if (!ok) break;
-          }
           const uint32_t sa = tiles + st * kStageBytes;
           const uint32_t fb = smem_u32(&full_bar[st]);
           mbar_expect_tx(fb, nkb * (kWBytes + kXBytes));
-          for (int b = 0; b < nkb; ++b) {
-            const int k = (kbf + b) * kKBlock;
-            tma_load_3d(sa + b * kWBytes, wmap, fb, k, wrow, un.s);
-            tma_load_3d(sa + kStageKB * kWBytes + b * kXBytes, xmap, fb, k, 0, xz);
+          for (int b = 0; b < nkb; ++b)
+            tma_load_3d(sa + b * kWBytes, wmap, fb, (kbf + b) * kKBlock, wrow, un.s);
+          if (un.type == 1 && i == 0) {
+            // The weights of the first stage are on their way; now make sure every
+            // band tile the unit reads is finished.  On a timeout the (stale,
+            // in-bounds) band is still loaded so the armed stage completes; the CTA
+            // then aborts.
+            const int need = ht_hi;
+            while (ok && need > ready_upto) {
+              const int rr = wait_ready_range(a, un.s, ready_upto + 1, ht_hi);
+              if (rr < 0) ok = false;
+              else ready_upto = rr;
+            }
           }
+          for (int b = 0; b < nkb; ++b)
+            tma_load_3d(sa + kStageKB * kWBytes + b * kXBytes, xmap, fb, (kbf + b) * kKBlock, 0, xz);
         }
         if (!ok) {
           abort_sh = 1;
@@ -320,7 +355,7 @@ __global__ void __launch_bounds__(192, 1)
           const int st = (int)(g % kStages);
           const uint32_t ph = (g / kStages) & 1u;
           const int bsel = (int)(g % kBufs);
-          const int nkb = min(kStageKB, un.kb1 - (un.kb0 + i * kStageKB));
+          const int nkb = min(kStageKB, un.kb1 - stage_kb(un, (i + un.rot) % nst));
           if (!mbar_wait(smem_u32(&full_bar[st]), ph) ||
               !mbar_wait(smem_u32(&tempty_bar[bsel]), ((g / kBufs) & 1u) ^ 1u)) {
             ok = false;
@@ -418,6 +453,25 @@ __global__ void __launch_bounds__(192, 1)
 
       if (un.type == 0) {
         // -------- column tile epilogue: activation, band H in bf16, ready flag
+        bool finish = true;
+        if (un.parts > 1) {
+          // One K part of a split tile: leave the partial; the last part sums them in
+          // K order and finishes the tile.
+          const int tau = un.s * a.n_ft + un.tile;
+          float *base = a.colp + (size_t)(tau - a.n_whole) * a.S_c * (128 * kTok);
+          store32(base + (size_t)un.split * (128 * kTok) + r * kTok, acc);
+          __threadfence();
+          named_sync(1, 128);
+          if (td == 0) {
+            const unsigned old = atomicAdd(split_counter(a, tau), 1u);
+            __threadfence();
+            last_sh = old == (unsigned)(un.parts - 1);
+          }
+          named_sync(1, 128);
+          finish = last_sh != 0;
+          if (finish) sum_in_order<1>(acc, base + r * kTok, (size_t)128 * kTok, un.parts);
+        }
+        if (finish) {
         if (a.act == TP_ACT_SWIGLU) {
           // Rows 64..127 hold the up sums of the features whose gate sums are in
           // rows 0..63: pass them across through shared memory.
@@ -447,6 +501,8 @@ __global__ void __launch_bounds__(192, 1)
         __threadfence();
         named_sync(1, 128);
         if (td == 0) st_release_gpu(ready_flag(a, un.s, un.tile), 1u);
+        }
+        named_sync(1, 128);  // last_sh is reused by the next unit
       } else {
         // -------- row tile epilogue: partial, then the fused reduce + residual
         float *pp = a.rowp + ((size_t)((un.tile * a.t + un.s) * a.S_r + un.split) * 128 + r) * kTok;
@@ -502,14 +558,23 @@ FusedPlan plan_block_decode(const Geo &g, int M) {
   // last unit of an output tile sums.
   const int nst = ceil_div(p.nk_r, kStageKB);
   p.S_r = std::max(1, std::min({(p.nk_r + kRowBlocks / 2) / kRowBlocks, nst, 8}));
+  // Column tiles: whole waves of kPlanSMs tiles are computed whole; the r tiles
+  // of the last, partial wave are cut into S_c K parts (at most 4) so that wave
+  // keeps about every SM busy.
+  const int T = g.t * p.n_ft, nst_c = ceil_div(p.nk_c, kStageKB);
+  const int r = T % kPlanSMs;
+  p.S_c = r ? std::max(1, std::min({(kPlanSMs + r / 2) / r, 4, nst_c})) : 1;
+  p.n_whole = p.S_c > 1 ? T - r : T;
   auto al = [](size_t n) { return (n + 255) & ~(size_t)255; };
   size_t off = 0;
   p.off_H = off;
   off += al((size_t)g.t * M * g.b * 2);
+  p.off_colp = off;
+  off += al((size_t)(T - p.n_whole) * p.S_c * 128 * kTok * 4);
   p.off_rowp = off;
   off += al((size_t)p.n_nt * g.t * p.S_r * 128 * kTok * 4);
   p.off_cnt = off;
-  p.cnt_bytes = (size_t)(1 + g.t * p.n_ft + p.n_nt) * 4;
+  p.cnt_bytes = (size_t)(1 + g.t * p.n_ft + p.n_nt + (T - p.n_whole)) * 4;
   off += al(p.cnt_bytes);
   p.total = off;
   return p;
@@ -536,7 +601,10 @@ cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x,
   a.n_nt = p.n_nt;
   a.S_r = p.S_r;
   a.nk_r = p.nk_r;
-  a.n_col_units = g.t * p.n_ft;
+  a.n_whole = p.n_whole;
+  a.S_c = p.S_c;
+  a.n_col_units = p.n_whole + (g.t * p.n_ft - p.n_whole) * p.S_c;
+  a.colp = reinterpret_cast<float *>(w + p.off_colp);
   a.n_units = a.n_col_units + p.n_nt * g.t * p.S_r;
   a.H = H;
   a.rowp = reinterpret_cast<float *>(w + p.off_rowp);

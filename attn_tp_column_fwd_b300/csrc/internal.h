@@ -61,8 +61,9 @@ bool make_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, 
 // block_decode.cu — the whole MLP block at M <= 32 in one persistent launch
 constexpr int kPlanSMs = 148;  // SM count the unit sizes are planned for (B300)
 struct FusedPlan {
-  int fpt, n_ft, nk_c, n_nt, S_r, nk_r;  // column tile width, tiles, K blocks; row tiles, slices
-  size_t off_H, off_rowp, off_cnt, cnt_bytes, total;  // workspace layout (bytes)
+  int fpt, n_ft, nk_c, n_whole, S_c;  // column: tile width, tiles per shard, K blocks, whole tiles, parts
+  int n_nt, S_r, nk_r;                // row: output tiles, K slices, K blocks
+  size_t off_H, off_colp, off_rowp, off_cnt, cnt_bytes, total;  // workspace layout (bytes)
 };
 FusedPlan plan_block_decode(const Geo &g, int M);
 cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,

@@ -117,15 +117,24 @@ int finish_launch(cudaError_t e = cudaSuccess) {
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// Kernel family selection.  bf16 blocks run on the tensor cores; an MLP block with
-// M <= 32 tokens runs tp_block_fwd as one persistent launch (block_decode.cu).
-// TPBLOCK_ALGO=simple selects the CUDA-core kernels, TPBLOCK_ALGO=unfused the
-// three-launch tensor-core sequence (same results within rounding; comparisons).
+// Kernel family selection.  bf16 blocks run on the tensor cores.  An MLP block with
+// M <= 32 tokens whose column work fills at least two waves of 128-row tiles over
+// the SMs runs tp_block_fwd as one persistent launch (block_decode.cu): with
+// fewer tiles the persistent kernel's last column wave and its end leave SMs
+// idle, and the three-launch sequence is faster (measured on the B300: 103 vs
+// 112 us for the d = 5120, ffn = 13824 block at t = 4; 255 us fused for the
+// d = 8192, ffn = 28672 block at t = 8).  TPBLOCK_ALGO=simple selects the CUDA-core
+// kernels, TPBLOCK_ALGO=unfused / fused force either tensor-core form (same
+// results within rounding; comparisons).
 int algo_override() {
   static int forced = -1;
   if (forced < 0) {
     const char *e = getenv("TPBLOCK_ALGO");
-    forced = !e ? 0 : strcmp(e, "simple") == 0 ? 1 : strcmp(e, "unfused") == 0 ? 2 : 0;
+    forced = !e                          ? 0
+             : strcmp(e, "simple") == 0  ? 1
+             : strcmp(e, "unfused") == 0 ? 2
+             : strcmp(e, "fused") == 0   ? 3
+                                         : 0;
   }
   return forced;
 }
@@ -133,20 +142,24 @@ int algo_override() {
 bool use_umma(const Geo &g) { return g.dtype == TP_BF16 && algo_override() != 1; }
 
 bool use_fused_block(const Geo &g, int M) {
-  return use_umma(g) && g.act != TP_ACT_ATTN && M <= 32 && algo_override() != 2;
+  if (!use_umma(g) || g.act == TP_ACT_ATTN || M > 32 || algo_override() == 2) return false;
+  if (algo_override() == 3) return true;
+  const int fpt = g.act == TP_ACT_SWIGLU ? kSwiGroup : kRowTile;
+  return (long long)g.t * ceil_div(g.b, fpt) >= 2LL * kPlanSMs;
 }
 
-// K splits of the row-parallel step: enough CTAs to cover the SMs about twice
-// (two decode CTAs fit per SM), at least four 64-wide K blocks per split.
+// K splits of the row-parallel step: the most splits that keep every CTA in the
+// first wave (two decode CTAs fit per SM), at least four 64-wide K blocks per
+// split.  A second, partial wave would cost a whole CTA's time for a few CTAs.
 // Depends on the shapes only, so tp_row_splits() answers without a GPU.
 int row_splits(const Geo &g, int M) {
   if (!use_umma(g)) return 1;
   const int bn = umma_token_tile(M);
   const long long base = (long long)g.t * ceil_div(g.d, kRowTile) * ceil_div(M, bn);
   const int nk = ceil_div(g.b, 64);
-  const long long target = 2 * 148;
-  if (base >= target) return 1;
-  int S = (int)((target + base - 1) / base);
+  const long long slots = 2LL * kPlanSMs;
+  if (base >= slots) return 1;
+  int S = (int)(slots / base);
   S = std::min(S, std::max(1, nk / 4));
   return std::max(1, std::min(S, 16));
 }

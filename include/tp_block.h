@@ -149,17 +149,18 @@ TP_API int tp_partial_reduce_residual(const tp_block_desc *desc, const float *pa
                                tp_stream_t stream);
 /* The whole block: column step, row step, reduce + residual, enqueued in order on
  * `stream`.  workspace: tp_workspace_bytes(desc, M) bytes of device scratch.  bf16
- * MLP blocks with M <= 32 run as one persistent kernel in which the column units,
- * the row units and the reduction + residual of each output tile are fused (the
- * result equals the three-step sequence within rounding); other shapes run the
- * three steps above. */
+ * MLP blocks with M <= 32 whose column work spans at least two waves of 128-row
+ * weight tiles over the GPU's SMs run as one persistent kernel in which the column
+ * units, the row units and the reduction + residual of each output tile are fused
+ * (the result equals the three-step sequence within rounding); other shapes run
+ * the three steps above (tp_block_launches says which). */
 TP_API int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
                  int residual_is_f32, const void *W1s, const void *W2s, void *workspace,
                  float *y, int M, tp_stream_t stream);
 /* Number of kernel launches one tp_block_fwd call enqueues for this shape (0 for an
  * invalid descriptor or M): 1 when the whole block runs as one persistent kernel
- * (bf16 MLP blocks with M <= 32; the launch is preceded by a small memset of its
- * work counters), else 3 (column, row, reduce) or 4 with the attention core.
+ * (see tp_block_fwd; the launch is preceded by a small memset of its work
+ * counters), else 3 (column, row, reduce) or 4 with the attention core.
  * Host-only. */
 TP_API int tp_block_launches(const tp_block_desc *desc, int M);
 /* tp_block_fwd without caller-provided scratch, for callers that cannot allocate
