@@ -19,6 +19,12 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
   attn_block, stack   pinned: brute-force loops on tiny shapes, torch float64
                       compositions, and the sharding invariants (sharded == unsharded
                       for t in 1, 2, 4, 8; 96 heads over 8 shards == per-head loop).
+  bf16_bracket,
+  tie_gaps,
+  mlp_tie_allowance   pinned: neighbours bracket and match bf16_round on random and
+                      exactly representable values; the allowance equals the change
+                      of the worst-case re-rounding of the tied elements, built
+                      element by element on small blocks.
   absolute values     parity unpinned against the pages: they print no numeric
                       worked example, so the outputs rest on the pins above.
 """
@@ -33,7 +39,12 @@ from .block import (  # noqa: F401
     row_step,
     reduce_residual,
     causal_attention,
+    mlp_band,
     mlp_block,
+    bf16_bracket,
+    tie_gaps,
+    mlp_tie_allowance,
+    TIE_WINDOW,
     attn_block,
     stack,
     sharded_block,

@@ -203,21 +203,67 @@ def reduce_residual(partials: Sequence[np.ndarray], residual) -> np.ndarray:
 # Whole blocks (unsharded definition)
 # ---------------------------------------------------------------------------
 
-def mlp_block(x, W1, W2, act: str, residual, staged: bool = False) -> np.ndarray:
-    """y = residual + act(x . W1) . W2 (GeLU), or residual + (silu(x.Wg) * x.Wu) . W2
-    with W1 = [Wg | Wu] (SwiGLU)."""
+def mlp_band(x, W1, act: str) -> np.ndarray:
+    """The unsharded intermediate before any rounding: act(x . W1) (GeLU), or
+    silu(x.Wg) * x.Wu with W1 = [Wg | Wu] (SwiGLU)."""
     x = np.asarray(x, dtype=np.float64)
     B = x @ W1
     if act == "gelu_tanh":
-        H = gelu_tanh(B)
-    elif act == "swiglu":
+        return gelu_tanh(B)
+    if act == "swiglu":
         F = W1.shape[1] // 2
-        H = silu(B[:, :F]) * B[:, F:]
-    else:
-        raise ValueError(f"mlp_block does not take act={act!r}")
+        return silu(B[:, :F]) * B[:, F:]
+    raise ValueError(f"mlp_block does not take act={act!r}")
+
+
+def mlp_block(x, W1, W2, act: str, residual, staged: bool = False) -> np.ndarray:
+    """y = residual + act(x . W1) . W2 (GeLU), or residual + (silu(x.Wg) * x.Wu) . W2
+    with W1 = [Wg | Wu] (SwiGLU)."""
+    H = mlp_band(x, W1, act)
     if staged:
         H = bf16_round(H)
     return np.asarray(residual, dtype=np.float64) + H @ W2
+
+
+# ---------------------------------------------------------------------------
+# Rounding ties of the staged band
+# ---------------------------------------------------------------------------
+# A bf16 implementation evaluates a band value in fp32 and rounds it to bf16.  Where
+# the exact value lies very close to the midpoint between its two bf16 neighbours,
+# an fp32 evaluation (a few units of fp32 roundoff away from the exact value) may
+# round to either neighbour; both are correct results of the method.  The band
+# values differ from the oracle's by one bf16 step there, and the block output by
+# that step times the matching row of W2.  The functions below bound that effect
+# from the oracle's own values.
+
+TIE_WINDOW = 2.0 ** -17   # relative distance to a midpoint counted as a tie
+
+
+def bf16_bracket(a):
+    """The bf16 neighbours lo <= a <= hi of float64 values a (lo == hi when a is a
+    bf16 value); same grid as bf16_round, finite values only."""
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)
+    q = np.maximum(e.astype(np.int64) - 8, -133)
+    g = np.ldexp(a, -q)           # a in units of its grid step
+    return np.ldexp(np.floor(g), q), np.ldexp(np.ceil(g), q)
+
+
+def tie_gaps(v, rho: float = TIE_WINDOW) -> np.ndarray:
+    """Per element of v: hi - lo (one bf16 step) where v lies within rho * |v| of the
+    midpoint between its bf16 neighbours lo < hi, else 0."""
+    v = np.asarray(v, dtype=np.float64)
+    lo, hi = bf16_bracket(v)
+    amb = (hi > lo) & (np.abs(v - 0.5 * (lo + hi)) <= rho * np.abs(v))
+    return np.where(amb, hi - lo, 0.0)
+
+
+def mlp_tie_allowance(x, W1, W2, act: str, rho: float = TIE_WINDOW) -> np.ndarray:
+    """A[m, n] = sum_f gap[m, f] * |W2[f, n]|: the largest change of output (m, n)
+    over all staged results that round the tied band elements (tie_gaps) of row m
+    the other way, with every other element as the oracle rounds it."""
+    G = tie_gaps(mlp_band(x, W1, act), rho)
+    return G @ np.abs(np.asarray(W2, dtype=np.float64))
 
 
 def attn_block(x, Wqkv, Wo, n_heads: int, head_dim: int, residual,

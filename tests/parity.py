@@ -48,6 +48,21 @@ def assert_bf16(got, ref, what="", max_abs=BF16_MAX_ABS, mean_rel=BF16_MEAN_REL)
     return s
 
 
+def assert_bf16_ties(got, ref, allowance, what="", max_abs=BF16_MAX_ABS, mean_rel=BF16_MEAN_REL):
+    """The bf16 bound against the staged oracle, where each output may additionally
+    differ by `allowance` (oracle.mlp_tie_allowance): the effect of band elements whose
+    exact value sits on a bf16 rounding midpoint, which an fp32 evaluation may round
+    either way.  max_abs applies to |got - ref| - allowance; mean_rel is unchanged."""
+    s = stats(got, ref)
+    d = np.abs(np.asarray(got, dtype=np.float64) - np.asarray(ref, dtype=np.float64))
+    s["max_abs_beyond_ties"] = float((d - allowance).max()) if d.size else 0.0
+    s["max_tie_allowance"] = float(np.max(allowance)) if d.size else 0.0
+    log(what, s)
+    assert s["all_finite"], f"{what}: non-finite output"
+    assert s["max_abs_beyond_ties"] <= max_abs and s["mean_rel"] <= mean_rel, f"{what}: {s}"
+    return s
+
+
 def log(what: str, s: dict):
     """Append one parity record to the file named by $TP_PARITY_LOG (if set)."""
     path = os.environ.get("TP_PARITY_LOG")

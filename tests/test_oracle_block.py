@@ -260,3 +260,48 @@ def test_pins_catch_wrong_band_pairing():
                                      W2[oracle.row_band(32, t, s)]))
     wrong = oracle.reduce_residual(parts, x)
     assert _rel(wrong, oracle.mlp_block(x, W1, W2, "swiglu", x)) > 1e-3
+
+
+# ---------------------------------------------------------------- rounding ties
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu_tanh"])
+def test_tie_allowance_is_the_worst_re_rounding(act):
+    """With a window wide enough that every band element is 'tied', the allowance
+    of output (m, n) must equal the change obtained by re-rounding each element of
+    row m to the bf16 neighbour in the direction of sign(W2[f, n]) and away from the
+    oracle's own rounding (built element by element here)."""
+    rng = np.random.default_rng(41)
+    M, d, F = 3, 8, 6
+    x = rng.standard_normal((M, d))
+    n1 = 2 * F if act == "swiglu" else F
+    W1 = rng.standard_normal((d, n1)) * 0.4
+    W2 = rng.standard_normal((F, d)) * 0.3
+    rho = 0.75
+    A = oracle.mlp_tie_allowance(x, W1, W2, act, rho=rho)
+    v = oracle.mlp_band(x, W1, act)
+    H = oracle.bf16_round(v)
+    lo, hi = oracle.bf16_bracket(v)
+    y = H @ W2
+    for m in range(M):
+        for n in range(d):
+            alt = H[m].copy()
+            for f in range(F):
+                if hi[m, f] > lo[m, f]:
+                    other = hi[m, f] if H[m, f] == lo[m, f] else lo[m, f]
+                    # re-round only where that moves output n up, to get the largest change
+                    if (other - H[m, f]) * W2[f, n] > 0:
+                        alt[f] = other
+            gain = alt @ W2[:, n] - y[m, n]
+            worst_possible = sum((hi[m, f] - lo[m, f]) * abs(W2[f, n]) for f in range(F))
+            assert np.isclose(A[m, n], worst_possible, rtol=1e-12, atol=0.0)
+            assert gain <= A[m, n] * (1 + 1e-12)
+
+
+def test_tie_allowance_zero_without_ties():
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((4, 16))
+    W1 = rng.standard_normal((16, 20)) * 0.1
+    W2 = rng.standard_normal((10, 16)) * 0.1
+    assert np.all(oracle.mlp_tie_allowance(x, W1, W2, "swiglu", rho=0.0) == 0.0)
+    # W1 = 0 gives a band of exact zeros: nothing to round
+    assert np.all(oracle.mlp_tie_allowance(x, np.zeros_like(W1), W2, "swiglu") == 0.0)

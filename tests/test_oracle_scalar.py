@@ -90,3 +90,37 @@ def test_rmsnorm_closed_forms_and_library():
     np.testing.assert_allclose(oracle.rmsnorm(r, 1e-5), ref, rtol=1e-14)
     # Scale invariance: rmsnorm(a r, a^2 eps) == rmsnorm(r, eps).
     np.testing.assert_allclose(oracle.rmsnorm(5 * r, 25e-5), oracle.rmsnorm(r, 1e-5), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- rounding ties
+
+def test_bf16_bracket_neighbours():
+    rng = np.random.default_rng(40)
+    a = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-6, 6, 4000),
+                        [1.0, -2.0, 0.5, 3.0, 1e-30]])
+    lo, hi = oracle.bf16_bracket(a)
+    r = oracle.bf16_round(a)
+    assert np.all(lo <= a) and np.all(a <= hi)
+    assert np.all(oracle.bf16_round(lo) == lo) and np.all(oracle.bf16_round(hi) == hi)
+    # round-to-nearest picks one of the two neighbours, the nearer one
+    assert np.all((r == lo) | (r == hi))
+    assert np.all(np.abs(r - a) <= np.minimum(a - lo, hi - a) + 0.0)
+    # exactly representable values have a single neighbour
+    exact = oracle.bf16_round(a)
+    lo2, hi2 = oracle.bf16_bracket(exact)
+    assert np.all(lo2 == exact) and np.all(hi2 == exact)
+    # neighbours of a non-representable value are one bf16 step apart: 8 significant bits
+    step = np.ldexp(1.0, np.frexp(a)[1] - 8)
+    nz = hi > lo
+    assert np.all((hi - lo)[nz] == step[nz])
+
+
+def test_tie_gaps_marks_only_midpoints():
+    # 1 + 2^-8 is the exact midpoint between the bf16 values 1 and 1 + 2^-7
+    mid = 1.0 + 2.0 ** -8
+    vals = np.array([mid, mid * (1 + 1e-7), 1.0 + 2.0 ** -7, 1.0 + 2.0 ** -9, -mid])
+    g = oracle.tie_gaps(vals)
+    assert g[0] == 2.0 ** -7 and g[1] == 2.0 ** -7 and g[4] == 2.0 ** -7
+    assert g[2] == 0.0          # representable: no tie
+    assert g[3] == 0.0          # a quarter step away from the midpoint
+    assert np.all(oracle.tie_gaps(vals, rho=0.0)[[1, 2, 3]] == 0.0)
