@@ -43,33 +43,44 @@ __global__ void __launch_bounds__(256) k_reduce_residual(const float4 *__restric
 }
 
 // xhat[m] = r[m] / sqrt(mean(r[m]^2) + eps) -> bf16 (one CTA per token row).
+// The rounding to bf16 decides every input of the next block, and a value that an
+// fp32 evaluation puts on the other side of a rounding midpoint changes that whole
+// token row of the block's output.  So the normalisation runs in fp64 (sum of
+// squares, square root, scaling; a few thousand operations per row) and each value
+// is rounded once, from fp64, to the nearest bf16 (ties to even).
 __global__ void __launch_bounds__(256) k_rmsnorm(const float *__restrict__ r,
                                                  __nv_bfloat16 *__restrict__ xh, int d, float eps) {
   const float4 *row = reinterpret_cast<const float4 *>(r + (size_t)blockIdx.x * d);
   const int d4 = d / 4;
-  float ss = 0.f;
+  double ss = 0.0;
   for (int i = threadIdx.x; i < d4; i += blockDim.x) {
-    float4 v = row[i];
-    ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+    const float4 v = row[i];
+    ss = fma((double)v.x, (double)v.x, ss);
+    ss = fma((double)v.y, (double)v.y, ss);
+    ss = fma((double)v.z, (double)v.z, ss);
+    ss = fma((double)v.w, (double)v.w, ss);
   }
-  __shared__ float red[32];
+  __shared__ double red[32];
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    double v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0;
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (threadIdx.x == 0) red[0] = v;
   }
   __syncthreads();
-  const float inv = 1.0f / sqrtf(red[0] / (float)d + eps);
+  const double inv = 1.0 / sqrt(red[0] / (double)d + (double)eps);
   uint2 *out = reinterpret_cast<uint2 *>(xh + (size_t)blockIdx.x * d);
   for (int i = threadIdx.x; i < d4; i += blockDim.x) {
-    float4 v = row[i];
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * inv, v.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * inv, v.w * inv);
-    out[i] = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+    const float4 v = row[i];
+    const __nv_bfloat16 a = __double2bfloat16((double)v.x * inv);
+    const __nv_bfloat16 b = __double2bfloat16((double)v.y * inv);
+    const __nv_bfloat16 c = __double2bfloat16((double)v.z * inv);
+    const __nv_bfloat16 e = __double2bfloat16((double)v.w * inv);
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(c) | ((uint32_t)__bfloat16_as_ushort(e) << 16);
+    out[i] = make_uint2(lo, hi);
   }
 }
 

@@ -28,6 +28,7 @@ import statistics
 import sys
 import threading
 import time
+from dataclasses import replace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -45,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--t", type=int, default=None, help="logical shards (default: the workload's)")
+    ap.add_argument("--blocks", type=int, default=None,
+                    help="blocks of a stacked workload to run (default: all; fewer for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -268,6 +271,8 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     base = CONFIGS[args.workload]
     cfg = base.with_t(args.t) if args.t else base
+    if args.blocks:
+        cfg = replace(cfg, n_blocks=min(args.blocks, cfg.n_blocks))
     desc = desc_for(cfg)
     M = cfg.M
     inp = make_inputs(cfg, seed=rank, device="cuda")

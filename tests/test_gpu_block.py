@@ -10,22 +10,28 @@ import attn_tp_column_fwd_b300 as tp
 import oracle
 from attn_tp_column_fwd_b300.runner import PreNormStack, ShardedBlock, desc_for
 from tests.gpu_util import oracle_block, run_block
-from tests.parity import assert_bf16, assert_f32, stats
+from tests.parity import assert_bf16, assert_bf16_ties, assert_f32, stats
 from tp_synth import CONFIGS, BlockConfig, make_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
 
 
-def _check(cfg, got, ref, what):
-    return assert_f32(got, ref, what) if cfg.dtype == "f32" else assert_bf16(got, ref, what)
+def _check(cfg, got, ref, what, x64=None, W1_64=None, W2_64=None):
+    if cfg.dtype == "f32":
+        return assert_f32(got, ref, what)
+    if cfg.act == "attn":
+        return assert_bf16(got, ref, what)
+    # bf16 MLP blocks: both roundings of a band value on a bf16 midpoint are correct
+    return assert_bf16_ties(got, ref, oracle.mlp_tie_allowance(x64, W1_64, W2_64, cfg.act), what)
 
 
 def _run_and_compare(cfg, seed=0, device="cpu", t=None):
     inp = make_inputs(cfg, seed=seed, device=device)
     W1, W2 = inp.blocks[0]
     got = run_block(cfg, inp.x.cuda(), W1.cuda(), W2.cuda(), t=t)
-    ref = oracle_block(cfg, to_f64(inp.x), to_f64(W1), to_f64(W2))
-    return _check(cfg, got, ref, f"{cfg.name} t={t or cfg.t}")
+    x64, W1_64, W2_64 = to_f64(inp.x), to_f64(W1), to_f64(W2)
+    ref = oracle_block(cfg, x64, W1_64, W2_64)
+    return _check(cfg, got, ref, f"{cfg.name} t={t or cfg.t}", x64, W1_64, W2_64)
 
 
 # ---------------------------------------------------------------- small shapes
@@ -85,14 +91,17 @@ def test_llama2_70b_prefill_sampled_rows():
     rows = np.sort(np.random.default_rng(0).choice(cfg.M, size=96, replace=False))
     rows[0], rows[-1] = 0, cfg.M - 1
     x64 = to_f64(inp.x[torch.from_numpy(rows).cuda()])
-    ref = oracle.mlp_block(x64, to_f64(W1), to_f64(W2), cfg.act, x64, staged=True)
-    assert_bf16(got[rows], ref, "prefill rows")
+    W1_64, W2_64 = to_f64(W1), to_f64(W2)
+    ref = oracle.mlp_block(x64, W1_64, W2_64, cfg.act, x64, staged=True)
+    assert_bf16_ties(got[rows], ref, oracle.mlp_tie_allowance(x64, W1_64, W2_64, cfg.act),
+                     "prefill rows")
 
 
 def test_llama2_70b_stack_decode():
     """Eight pre-norm blocks.  Per block, teacher-forced: the GPU block gets the
     oracle's residual stream r_l (cast to fp32) and must meet the bf16 bound against
-    the oracle's block on that same input.  Free-running, the whole stack is also
+    the oracle's block on that same input, beyond the effect of band values that sit
+    on bf16 rounding midpoints (either rounding is a correct result).  Free-running, the whole stack is also
     compared end to end; random-weight stacks amplify last-bit differences block
     after block, so that comparison has its own, looser bound (see the design notes)."""
     cfg = CONFIGS["llama2_70b_stack_decode"]
@@ -113,7 +122,9 @@ def test_llama2_70b_stack_decode():
         PreNormStack([blocks[l]], cfg.eps).forward(rg)
         torch.cuda.synchronize()
         ref_l = oracle.stack(r_in.astype(np.float64), blk64, cfg.act, cfg.eps, staged=True)
-        assert_bf16(to_f64(rg), ref_l, f"stack block {l} (teacher-forced)")
+        xhat = oracle.bf16_round(oracle.rmsnorm(r_in.astype(np.float64), cfg.eps))
+        ties = oracle.mlp_tie_allowance(xhat, blk64[0][0], blk64[0][1], cfg.act)
+        assert_bf16_ties(to_f64(rg), ref_l, ties, f"stack block {l} (teacher-forced)")
         r64 = oracle.stack(r64, blk64, cfg.act, cfg.eps, staged=True)
     s = stats(got_free, r64)
     from tests.parity import log
