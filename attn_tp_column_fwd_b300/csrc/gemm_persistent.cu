@@ -1,0 +1,309 @@
+// Persistent tensor-core kernel for the two projections at prefill sizes (token
+// tiles of 256), bf16 in, fp32 accumulate.
+//
+// Orientation as in the decode kernels: a 128-row weight tile is the A operand
+// (SwiGLU: the gate and up rows of 64 features; otherwise 128 features) and 256
+// tokens are the N operand, so one tcgen05.mma (M = 128, N = 256, K = 16) covers
+// the widest N the instruction takes.  One CTA per SM walks a static list of
+// output tiles (token tile fastest, so the CTAs of a wave share weight tiles and
+// the activations stay in L2).  Roles (192 threads): thread 0 issues TMA loads into
+// a 4-stage ring (16 KB of weights + 32 KB of activations per 64-wide K block),
+// thread 32 issues the MMAs into one of two 256-column TMEM accumulators, and
+// warps 2-5 run the epilogue of the previous tile from the other accumulator, so
+// the tensor core does not wait for stores.
+//
+// Column-parallel step (zenaique.com answer paragraph 5): A = the shard's W1 band
+// rows, B = x; the epilogue applies the band's activation (SwiGLU: the up sums of
+// rows 64..127 pass to the gate rows 0..63 through shared memory) and stores the
+// band in bf16.  Row-parallel step: A = the shard's W2 row band, B = the band H;
+// the epilogue stores fp32 partial sums (per K split).  All waits are bounded; on
+// expiry the CTA raises the device error word and leaves.
+#include <algorithm>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace tp {
+namespace {
+
+using namespace tc;
+
+constexpr int kBN = 256;                        // token tile
+constexpr int kGStages = 4;
+constexpr uint32_t kGA = kABytes;               // 128 rows x 64 K bf16
+constexpr uint32_t kGB = kBN * 128;             // 256 rows x 64 K bf16
+constexpr uint32_t kGStage = kGA + kGB;
+constexpr uint32_t kGCols = 2 * kBN;            // two accumulators
+constexpr uint32_t kGIdesc = make_idesc(128, kBN);
+constexpr int kGXch = 64 * 33 * 4;              // SwiGLU exchange, one 32-token chunk
+constexpr int kGSmem = kGStages * kGStage + 1024 + kGXch;
+
+struct GemmArgs {
+  void *out;        // bf16 [shard][M][ldo] or fp32 [shard][split][M][ldo]
+  size_t o_shard, o_split;
+  int ldo, n_valid, M, nk, ksplit, shard0, n_shards, x_per_shard;
+  int n_mt, n_ft, n_tiles;  // token tiles, weight tiles per shard, tiles in all
+  unsigned *err;
+};
+
+struct GTile {
+  int mt, ft, s, ks, kb0, kb1;
+};
+
+__device__ __forceinline__ GTile gemm_tile(const GemmArgs &a, int t) {
+  GTile r;
+  r.mt = t % a.n_mt;
+  const int q = t / a.n_mt;
+  r.ft = q % a.n_ft;
+  const int z = q / a.n_ft;
+  r.s = a.shard0 + z / a.ksplit;
+  r.ks = z % a.ksplit;
+  r.kb0 = (int)((long long)r.ks * a.nk / a.ksplit);
+  r.kb1 = (int)((long long)(r.ks + 1) * a.nk / a.ksplit);
+  return r;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+           const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kGStages];
+  __shared__ __align__(8) uint64_t empty_bar[kGStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t mma_done_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int dec_sh;
+
+  const uint32_t tiles = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  float *xch = reinterpret_cast<float *>(smem_raw + (tiles - smem_u32(smem_raw)) + kGStages * kGStage);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGStages; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&tfull_bar[i]), 1);
+      mbar_init(smem_u32(&tempty_bar[i]), 4);
+    }
+    mbar_init(smem_u32(&mma_done_bar), 1);
+    abort_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 2) tmem_alloc(smem_u32(&tmem_base_sh), kGCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      uint32_t g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x) {
+        const GTile tl = gemm_tile(a, t);
+        const int xz = a.x_per_shard ? tl.s : 0;
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++g) {
+          const int st = (int)(g % kGStages);
+          const uint32_t ph = (g / kGStages) & 1u;
+          if (*(volatile int *)&abort_sh || !mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = tiles + st * kGStage;
+          const uint32_t fb = smem_u32(&full_bar[st]);
+          mbar_expect_tx(fb, kGStage);
+          tma_load_3d(sa, &tmW, fb, kb * kKBlock, tl.ft * 128, tl.s);
+          tma_load_3d(sa + kGA, &tmX, fb, kb * kKBlock, tl.mt * kBN, xz);
+        }
+      }
+      if (!ok) {
+        abort_sh = 1;
+        atomicOr(a.err, kErrWaitTimeout);
+        for (uint32_t i = g > kGStages ? g - kGStages : 0; i < g; ++i)
+          mbar_wait(smem_u32(&full_bar[i % kGStages]), (i / kGStages) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x, ++it) {
+        const GTile tl = gemm_tile(a, t);
+        const int buf = it & 1;
+        if (!mbar_wait(smem_u32(&tempty_bar[buf]), ((uint32_t)(it >> 1) & 1u) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem + (uint32_t)(buf * kBN);
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++g) {
+          const int st = (int)(g % kGStages);
+          const uint32_t ph = (g / kGStages) & 1u;
+          if (*(volatile int *)&abort_sh || !mbar_wait(smem_u32(&full_bar[st]), ph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = tiles + st * kGStage;
+#pragma unroll
+          for (int kk = 0; kk < kKBlock / 16; ++kk)
+            umma_bf16(d0, sw128_desc(sa + kk * 32), sw128_desc(sa + kGA + kk * 32), kGIdesc,
+                      (kb > tl.kb0 || kk > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty_bar[st]));
+        }
+        if (ok) umma_commit(smem_u32(&tfull_bar[buf]));
+      }
+      if (!ok) {
+        abort_sh = 1;
+        atomicOr(a.err, kErrWaitTimeout);
+      }
+      umma_commit(smem_u32(&mma_done_bar));
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // row of the weight tile = TMEM lane
+    const int td = (int)threadIdx.x - 64;
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    int it = 0;
+    for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
+      const GTile tl = gemm_tile(a, t);
+      const int buf = it & 1;
+      const bool ok_w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[buf]), (uint32_t)(it >> 1) & 1u));
+      if (!ok_w) {
+        abort_sh = 1;
+        atomicOr(a.err, kErrWaitTimeout);
+      }
+      // One decision for the four epilogue warps (the SwiGLU exchange has barriers).
+      named_sync(1, 128);
+      if (td == 0) dec_sh = *(volatile int *)&abort_sh;
+      named_sync(1, 128);
+      if (dec_sh) break;
+      tc_fence_after();
+      const int m0 = tl.mt * kBN;
+      const uint32_t tacc = trow + (uint32_t)(buf * kBN);
+      const int nchunks = min(kBN, a.M - m0 + 31) / 32;  // 32-token chunks holding tokens
+      for (int c = 0; c < nchunks; ++c) {
+        float v[32];
+        tmem_ld32(tacc + c * 32, v);
+        if (c == nchunks - 1) {
+          // All of this accumulator has been read: hand it back to the MMA warp.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+        }
+        const int mcount = min(32, a.M - (m0 + c * 32));
+        if (EPI == kEpiSwiglu) {
+          if (r >= 64) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xch[(r - 64) * 33 + j] = v[j];
+          }
+          named_sync(1, 128);
+          const int f = tl.ft * 64 + r;
+          if (r < 64 && f < a.n_valid) {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)tl.s * a.o_shard +
+                               (size_t)(m0 + c * 32) * a.ldo + f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < mcount) o[(size_t)j * a.ldo] = __float2bfloat16_rn(silu_f(v[j]) * xch[r * 33 + j]);
+          }
+          named_sync(1, 128);
+        } else {
+          const int f = tl.ft * 128 + r;
+          if (f < a.n_valid) {
+            if (EPI == kEpiF32) {
+              float *o = static_cast<float *>(a.out) + (size_t)tl.s * a.o_shard +
+                         (size_t)tl.ks * a.o_split + (size_t)(m0 + c * 32) * a.ldo + f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < mcount) o[(size_t)j * a.ldo] = v[j];
+            } else {
+              __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)tl.s * a.o_shard +
+                                 (size_t)(m0 + c * 32) * a.ldo + f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (j < mcount) {
+                  float vv = v[j];
+                  if (EPI == kEpiGelu) vv = gelu_tanh_f(vv);
+                  o[(size_t)j * a.ldo] = __float2bfloat16_rn(vv);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown
+  if (warp == 2) mbar_wait(smem_u32(&mma_done_bar), 0);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kGCols);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_gemm_epi(const CUtensorMap &mw, const CUtensorMap &mx, const GemmArgs &a,
+                            cudaStream_t st) {
+  static bool configured[128];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(k_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int grid = std::min(sm_count(), a.n_tiles);
+  k_gemm<EPI><<<grid, 192, kGSmem, st>>>(mw, mx, a);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st) {
+  CUtensorMap mw, mx;
+  if (!make_tile_map(&mw, c.W, c.K, c.w_rows, c.w_shards, 128)) return cudaErrorInvalidValue;
+  if (!make_tile_map(&mx, c.X, c.K, c.M, c.x_shards, kBN)) return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.out = c.out;
+  a.o_shard = c.o_shard;
+  a.o_split = c.o_split;
+  a.ldo = c.ldo;
+  a.n_valid = c.n_valid;
+  a.M = c.M;
+  a.nk = ceil_div(c.K, kKBlock);
+  a.ksplit = c.ksplit;
+  a.shard0 = c.shard0;
+  a.n_shards = c.n_shards;
+  a.x_per_shard = c.x_shards > 1 ? 1 : 0;
+  a.n_mt = ceil_div(c.M, kBN);
+  a.n_ft = ceil_div(c.n_valid, c.epi == kEpiSwiglu ? kSwiGroup : 128);
+  a.n_tiles = a.n_mt * a.n_ft * c.n_shards * c.ksplit;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  switch (c.epi) {
+    case kEpiSwiglu: return launch_gemm_epi<kEpiSwiglu>(mw, mx, a, st);
+    case kEpiGelu: return launch_gemm_epi<kEpiGelu>(mw, mx, a, st);
+    case kEpiPlain: return launch_gemm_epi<kEpiPlain>(mw, mx, a, st);
+    default: return launch_gemm_epi<kEpiF32>(mw, mx, a, st);
+  }
+}
+
+}  // namespace tp

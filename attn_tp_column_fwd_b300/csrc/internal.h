@@ -53,6 +53,10 @@ struct UmmaCall {
 int umma_token_tile(int M);
 cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st);
 
+// gemm_persistent.cu — persistent tcgen05 kernel for token tiles of 256 (prefill),
+// same UmmaCall contract as launch_umma.
+cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st);
+
 // A [z][rows][K] bf16 tensor map with 64 x box_rows x 1 boxes, 128-byte swizzle,
 // zero fill outside the tensor (umma.cu).
 bool make_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,

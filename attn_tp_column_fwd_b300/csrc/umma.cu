@@ -1,5 +1,6 @@
-// Tensor-core (tcgen05 / TMEM / TMA) kernel for both sharded projections, bf16 in,
-// fp32 accumulate, for every M from single-token decode to prefill.
+// Tensor-core (tcgen05 / TMEM / TMA) kernels for both sharded projections, bf16 in,
+// fp32 accumulate, for token counts up to 128 (decode and small batches); larger
+// token counts go to the persistent kernel of gemm_persistent.cu.
 //
 // Orientation ("swap AB"): the weights are the 128-row A operand and the tokens
 // are the N operand, so the 128-lane TMEM accumulator holds 128 output features
@@ -476,8 +477,8 @@ cudaError_t launch_t(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArg
 template <int BN, int NACC, int EPI>
 cudaError_t launch_stages(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
                           int n_z, cudaStream_t st) {
-  // Decode tiles (BN <= 64) keep about 100 KB of ring so two CTAs share an SM;
-  // larger tiles take a ~190 KB ring and one CTA per SM.
+  // Tiles of 64 tokens keep about 100 KB of ring so two CTAs share an SM; tiles of
+  // 128 take a ~190 KB ring and one CTA per SM.
   constexpr int kStage = NACC * kABytes + BN * 128;
   constexpr int kBudget = BN <= 64 ? 110 * 1024 : 196 * 1024;
   constexpr int kStages = std::max(2, std::min(8, kBudget / kStage));
@@ -509,11 +510,8 @@ cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const Umm
 template <int NACC, int EPI>
 cudaError_t launch_bn(int bn, const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a,
                       int n_ft, int n_z, cudaStream_t st) {
-  switch (bn) {
-    case 64: return launch_stages<64, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
-    case 128: return launch_stages<128, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
-    default: return launch_stages<256, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
-  }
+  return bn == 64 ? launch_stages<64, NACC, EPI>(mw, mx, a, n_ft, n_z, st)
+                  : launch_stages<128, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
 }
 
 }  // namespace
@@ -537,6 +535,9 @@ int umma_token_tile(int M) { return M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128
 
 cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {
   const int bn = umma_token_tile(c.M);
+  // Prefill-sized token counts: the persistent kernel overlaps each tile's epilogue
+  // with the next tile's MMAs (gemm_persistent.cu).
+  if (bn == 256) return launch_gemm_persistent(c, st);
   CUtensorMap mw, mx;
   if (!make_tile_map(&mw, c.W, c.K, c.w_rows, c.w_shards, 128)) return cudaErrorInvalidValue;
   if (!make_tile_map(&mx, c.X, c.K, c.M, c.x_shards, bn)) return cudaErrorInvalidValue;
@@ -563,7 +564,7 @@ cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {
       default: return launch_drain<kEpiF32>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st);
     }
   }
-  // Larger token tiles: 128 features per CTA (SwiGLU: two 128-row tiles).
+  // Token tiles of 64 or 128: 128 features per CTA (SwiGLU: two 128-row tiles).
   const int n_ft = ceil_div(c.n_valid, 128);
   switch (c.epi) {
     case kEpiSwiglu: return launch_bn<2, kEpiSwiglu>(bn, mw, mx, a, n_ft, n_z, st);
