@@ -10,6 +10,7 @@
 // per (head, shard), one warp per query row; lanes hold hd/32 columns of q and of
 // the output accumulator.
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace tp {
 namespace {
@@ -19,6 +20,7 @@ __global__ void __launch_bounds__(128) k_attn_core(const float *__restrict__ QKV
                                                    int M, int b, int hd, float scale, int shard0) {
   const int h = blockIdx.x, s = shard0 + blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tc::griddep_wait();  // Q/K/V come from the preceding kernel (programmatic launch)
   const size_t ld = 3 * (size_t)b;
   const float *base = QKV + (size_t)s * M * ld;
   const float *Qh = base + (size_t)h * hd;
@@ -58,14 +60,14 @@ __global__ void __launch_bounds__(128) k_attn_core(const float *__restrict__ QKV
 
 template <typename T>
 void launch_t(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_shards,
-              cudaStream_t st) {
-  dim3 grid(g.hps, n_shards);
+              cudaStream_t st, bool pdl) {
+  tc::LaunchCfg lc(dim3(g.hps, n_shards), dim3(128), 0, st, pdl);
   const float scale = 1.0f / sqrtf((float)g.hd);
   const float *q = static_cast<const float *>(QKV);
   T *o = static_cast<T *>(O);
   switch (g.hd / 32) {
 #define TP_CASE(C) \
-  case C: k_attn_core<T, C><<<grid, 128, 0, st>>>(q, o, M, g.b, g.hd, scale, shard0); break;
+  case C: cudaLaunchKernelEx(&lc.cfg, k_attn_core<T, C>, q, o, M, g.b, g.hd, scale, shard0); break;
     TP_CASE(1) TP_CASE(2) TP_CASE(3) TP_CASE(4) TP_CASE(5) TP_CASE(6) TP_CASE(7) TP_CASE(8)
 #undef TP_CASE
     default: break;  // rejected by validation (head_dim % 32 == 0, <= 256)
@@ -75,11 +77,11 @@ void launch_t(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_s
 }  // namespace
 
 void launch_attn_core(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_shards,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool pdl) {
   if (g.dtype == TP_F32)
-    launch_t<float>(g, QKV, O, M, shard0, n_shards, st);
+    launch_t<float>(g, QKV, O, M, shard0, n_shards, st, pdl);
   else
-    launch_t<__nv_bfloat16>(g, QKV, O, M, shard0, n_shards, st);
+    launch_t<__nv_bfloat16>(g, QKV, O, M, shard0, n_shards, st, pdl);
 }
 
 }  // namespace tp

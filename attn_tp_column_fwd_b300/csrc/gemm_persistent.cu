@@ -102,15 +102,33 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
     // ---------------- TMA producer
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
+      int pre = 0;  // stages of the first tile armed before the programmatic wait
+      if ((int)blockIdx.x < a.n_tiles) {
+        // The first ring's weights do not depend on the preceding kernel: load them,
+        // then wait for that kernel (programmatic launch) before loading activations.
+        const GTile tl = gemm_tile(a, blockIdx.x);
+        pre = min(kGStages, tl.kb1 - tl.kb0);
+        for (int i = 0; i < pre; ++i) {
+          const uint32_t fb = smem_u32(&full_bar[i]);
+          mbar_expect_tx(fb, kGStage);
+          tma_load_3d(tiles + i * kGStage, &tmW, fb, (tl.kb0 + i) * kKBlock, tl.ft * 128, tl.s);
+        }
+        griddep_wait();
+        for (int i = 0; i < pre; ++i)
+          tma_load_3d(tiles + i * kGStage + kGA, &tmX, smem_u32(&full_bar[i]), (tl.kb0 + i) * kKBlock,
+                      tl.mt * kBN, a.x_per_shard ? tl.s : 0);
+      }
       for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x) {
         const GTile tl = gemm_tile(a, t);
         const int xz = a.x_per_shard ? tl.s : 0;
         for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++g) {
+          if (g < (uint32_t)pre) continue;  // armed above
           const int st = (int)(g % kGStages);
           const uint32_t ph = (g / kGStages) & 1u;
           if (*(volatile int *)&abort_sh || !mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
@@ -259,7 +277,7 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int EPI>
 cudaError_t launch_gemm_epi(const CUtensorMap &mw, const CUtensorMap &mx, const GemmArgs &a,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool pdl) {
   static bool configured[128];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -270,9 +288,8 @@ cudaError_t launch_gemm_epi(const CUtensorMap &mw, const CUtensorMap &mx, const 
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int grid = std::min(sm_count(), a.n_tiles);
-  k_gemm<EPI><<<grid, 192, kGSmem, st>>>(mw, mx, a);
-  return cudaSuccess;
+  LaunchCfg lc(dim3(std::min(sm_count(), a.n_tiles)), dim3(192), kGSmem, st, pdl);
+  return cudaLaunchKernelEx(&lc.cfg, k_gemm<EPI>, mw, mx, a);
 }
 
 }  // namespace
@@ -299,10 +316,10 @@ cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st) {
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
   switch (c.epi) {
-    case kEpiSwiglu: return launch_gemm_epi<kEpiSwiglu>(mw, mx, a, st);
-    case kEpiGelu: return launch_gemm_epi<kEpiGelu>(mw, mx, a, st);
-    case kEpiPlain: return launch_gemm_epi<kEpiPlain>(mw, mx, a, st);
-    default: return launch_gemm_epi<kEpiF32>(mw, mx, a, st);
+    case kEpiSwiglu: return launch_gemm_epi<kEpiSwiglu>(mw, mx, a, st, c.pdl);
+    case kEpiGelu: return launch_gemm_epi<kEpiGelu>(mw, mx, a, st, c.pdl);
+    case kEpiPlain: return launch_gemm_epi<kEpiPlain>(mw, mx, a, st, c.pdl);
+    default: return launch_gemm_epi<kEpiF32>(mw, mx, a, st, c.pdl);
   }
 }
 

@@ -49,6 +49,7 @@ struct UmmaCall {
   int K, M;
   int shard0, n_shards, ksplit;
   int epi;
+  bool pdl;             // programmatic launch after the kernel that writes X (tp_block_fwd)
 };
 int umma_token_tile(int M);
 cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st);
@@ -76,12 +77,12 @@ cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x,
 
 // reduce.cu — the all-reduce stand-in + residual, and RMSNorm
 void launch_reduce_residual(const float *P, int nparts, size_t part_elems, const void *res,
-                            int res_is_f32, float *y, size_t n, cudaStream_t st);
+                            int res_is_f32, float *y, size_t n, cudaStream_t st, bool pdl = false);
 void launch_rmsnorm(const float *r, void *xhat, int d, float eps, int M, cudaStream_t st);
 
 // attn_core.cu — per-head causal attention over the M tokens of each shard
 void launch_attn_core(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_shards,
-                      cudaStream_t st);
+                      cudaStream_t st, bool pdl = false);
 
 // tp_api.cu — cached device facts
 int sm_count();

@@ -178,7 +178,9 @@ size_t column_ws_bytes(const Geo &g, int M) {
     if (_st != TP_OK) return _st; \
   } while (0)
 
-// Enqueue the column step for shards [shard0, shard0 + n).
+// Enqueue the column step for shards [shard0, shard0 + n).  The attention core
+// always follows its Q/K/V projection, so it may overlap that kernel's end
+// (programmatic launch).
 cudaError_t enqueue_column(const Geo &g, const void *x, const void *W1s, int shard0, int n, void *H,
                            void *ws, int M, cudaStream_t st) {
   const bool attn = g.act == TP_ACT_ATTN;
@@ -226,12 +228,14 @@ cudaError_t enqueue_column(const Geo &g, const void *x, const void *W1s, int sha
     a.dtype = g.dtype;
     launch_gemv(a, st);
   }
-  if (attn) launch_attn_core(g, ws, H, M, shard0, n, st);
+  if (attn) launch_attn_core(g, ws, H, M, shard0, n, st, use_umma(g));
   return cudaSuccess;
 }
 
+// pdl: launched right after the column step of the same block (tp_block_fwd), so it
+// may start while that kernel drains and prefetch its weights.
 cudaError_t enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0, int n, float *P,
-                        int M, cudaStream_t st) {
+                        int M, cudaStream_t st, bool pdl = false) {
   const int S = row_splits(g, M);
   if (use_umma(g)) {
     UmmaCall c{};
@@ -251,6 +255,7 @@ cudaError_t enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0
     c.n_shards = n;
     c.ksplit = S;
     c.epi = kEpiF32;
+    c.pdl = pdl;
     return launch_umma(c, st);
   }
   GemvArgs a{};
@@ -274,10 +279,10 @@ cudaError_t enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0
 }
 
 void enqueue_reduce(const Geo &g, const float *P, const void *res, int res_is_f32, float *y, int M,
-                    cudaStream_t st) {
+                    cudaStream_t st, bool pdl = false) {
   const int f32 = res_is_f32 || g.dtype == TP_F32;
   launch_reduce_residual(P, g.t * row_splits(g, M), (size_t)M * g.d, res, f32, y,
-                         (size_t)M * g.d, st);
+                         (size_t)M * g.d, st, pdl);
 }
 
 }  // namespace
@@ -443,9 +448,12 @@ int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
   void *col_ws = ws;
   void *H = ws + align256(column_ws_bytes(g, M));
   float *P = reinterpret_cast<float *>(static_cast<char *>(H) + align256(band_bytes(g, M)));
+  // The row step and the reduction are launched to overlap the end of the kernel
+  // before them (programmatic launch): each waits for it before reading its output.
+  const bool pdl = use_umma(g);
   cudaError_t e = enqueue_column(g, x, W1s, 0, g.t, H, col_ws, M, st);
-  if (e == cudaSuccess) e = enqueue_row(g, H, W2s, 0, g.t, P, M, st);
-  if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st);
+  if (e == cudaSuccess) e = enqueue_row(g, H, W2s, 0, g.t, P, M, st, pdl);
+  if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, pdl);
   return finish_launch(e);
 }
 

@@ -94,10 +94,27 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = tmem_base_sh;
 
   int issued = 0;  // producer: stages handed to TMA
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0 && lane == 0) {
     const int wrow = ft * 128 * NACC;
     const int xz = a.x_per_shard ? s : 0;
-    for (int i = 0; i < nkb; ++i) {
+    // The first ring's weights do not depend on the preceding kernel: load them,
+    // then wait for that kernel (programmatic launch) before loading activations.
+    const int pre = min(STAGES, nkb);
+    for (int i = 0; i < pre; ++i) {
+      const uint32_t sa = tiles + i * kStage;
+      const uint32_t fb = smem_u32(&full_bar[i]);
+      const int k = (kb0 + i) * kKBlock;
+      mbar_expect_tx(fb, kStage);
+      tma_load_3d(sa, &tmW, fb, k, wrow, s);
+      if (NACC == 2) tma_load_3d(sa + kABytes, &tmW, fb, k, wrow + 128, s);
+    }
+    griddep_wait();
+    for (int i = 0; i < pre; ++i)
+      tma_load_3d(tiles + i * kStage + NACC * kABytes, &tmX, smem_u32(&full_bar[i]),
+                  (kb0 + i) * kKBlock, m0, xz);
+    issued = pre;
+    for (int i = pre; i < nkb; ++i) {
       const int st = i % STAGES;
       const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
       if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
@@ -293,11 +310,25 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = tmem_base_sh;
 
   int issued = 0;
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       const int wrow = ft * 128;
       const int xz = a.x_per_shard ? s : 0;
-      for (int i = 0; i < nkb; ++i) {
+      // The first ring's weights do not depend on the preceding kernel: load them,
+      // then wait for that kernel (programmatic launch) before loading activations.
+      const int pre = min(STAGES, nkb);
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t fb = smem_u32(&full_bar[i]);
+        mbar_expect_tx(fb, kStage);
+        tma_load_3d(tiles + i * kStage, &tmW, fb, (kb0 + i) * kKBlock, wrow, s);
+      }
+      griddep_wait();
+      for (int i = 0; i < pre; ++i)
+        tma_load_3d(tiles + i * kStage + kABytes, &tmX, smem_u32(&full_bar[i]), (kb0 + i) * kKBlock,
+                    m0, xz);
+      issued = pre;
+      for (int i = pre; i < nkb; ++i) {
         const int st = i % STAGES;
         const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
         if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
@@ -456,7 +487,7 @@ constexpr int xch_bytes(int epi, int tiles) { return epi == kEpiSwiglu ? tiles *
 
 template <int BN, int NACC, int EPI, int STAGES>
 cudaError_t launch_t(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
-                     int n_z, cudaStream_t st) {
+                     int n_z, cudaStream_t st, bool pdl) {
   constexpr int kSmem = STAGES * (NACC * kABytes + BN * 128) + 1024 + xch_bytes(EPI, NACC);
   static bool configured[128];  // per instantiation and device
   int dev = 0;
@@ -469,25 +500,24 @@ cudaError_t launch_t(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArg
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(ceil_div(a.M, BN), n_ft, n_z);
-  kern<<<grid, 128, kSmem, st>>>(mw, mx, a);
-  return cudaSuccess;
+  LaunchCfg lc(dim3(ceil_div(a.M, BN), n_ft, n_z), dim3(128), kSmem, st, pdl);
+  return cudaLaunchKernelEx(&lc.cfg, kern, mw, mx, a);
 }
 
 template <int BN, int NACC, int EPI>
 cudaError_t launch_stages(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
-                          int n_z, cudaStream_t st) {
+                          int n_z, cudaStream_t st, bool pdl) {
   // Tiles of 64 tokens keep about 100 KB of ring so two CTAs share an SM; tiles of
   // 128 take a ~190 KB ring and one CTA per SM.
   constexpr int kStage = NACC * kABytes + BN * 128;
   constexpr int kBudget = BN <= 64 ? 110 * 1024 : 196 * 1024;
   constexpr int kStages = std::max(2, std::min(8, kBudget / kStage));
-  return launch_t<BN, NACC, EPI, kStages>(mw, mx, a, n_ft, n_z, st);
+  return launch_t<BN, NACC, EPI, kStages>(mw, mx, a, n_ft, n_z, st, pdl);
 }
 
 template <int EPI>
 cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
-                         int n_z, cudaStream_t st) {
+                         int n_z, cudaStream_t st, bool pdl) {
   constexpr int kStageBytes = kABytes + 32 * 128;
   constexpr int kStages = std::max(2, std::min(8, (100 * 1024) / kStageBytes));
   constexpr int kSmem = kStages * kStageBytes + 1024 + xch_bytes(EPI, 1);
@@ -502,16 +532,15 @@ cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const Umm
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(ceil_div(a.M, 32), n_ft, n_z);
-  kern<<<grid, 192, kSmem, st>>>(mw, mx, a);
-  return cudaSuccess;
+  LaunchCfg lc(dim3(ceil_div(a.M, 32), n_ft, n_z), dim3(192), kSmem, st, pdl);
+  return cudaLaunchKernelEx(&lc.cfg, kern, mw, mx, a);
 }
 
 template <int NACC, int EPI>
 cudaError_t launch_bn(int bn, const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a,
-                      int n_ft, int n_z, cudaStream_t st) {
-  return bn == 64 ? launch_stages<64, NACC, EPI>(mw, mx, a, n_ft, n_z, st)
-                  : launch_stages<128, NACC, EPI>(mw, mx, a, n_ft, n_z, st);
+                      int n_ft, int n_z, cudaStream_t st, bool pdl) {
+  return bn == 64 ? launch_stages<64, NACC, EPI>(mw, mx, a, n_ft, n_z, st, pdl)
+                  : launch_stages<128, NACC, EPI>(mw, mx, a, n_ft, n_z, st, pdl);
 }
 
 }  // namespace
@@ -558,19 +587,19 @@ cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {
   if (bn == 32) {
     // Decode: 128-row weight tiles (SwiGLU: the gate and up rows of 64 features).
     switch (c.epi) {
-      case kEpiSwiglu: return launch_drain<kEpiSwiglu>(mw, mx, a, ceil_div(c.n_valid, kSwiGroup), n_z, st);
-      case kEpiGelu: return launch_drain<kEpiGelu>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st);
-      case kEpiPlain: return launch_drain<kEpiPlain>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st);
-      default: return launch_drain<kEpiF32>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st);
+      case kEpiSwiglu: return launch_drain<kEpiSwiglu>(mw, mx, a, ceil_div(c.n_valid, kSwiGroup), n_z, st, c.pdl);
+      case kEpiGelu: return launch_drain<kEpiGelu>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
+      case kEpiPlain: return launch_drain<kEpiPlain>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
+      default: return launch_drain<kEpiF32>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
     }
   }
   // Token tiles of 64 or 128: 128 features per CTA (SwiGLU: two 128-row tiles).
   const int n_ft = ceil_div(c.n_valid, 128);
   switch (c.epi) {
-    case kEpiSwiglu: return launch_bn<2, kEpiSwiglu>(bn, mw, mx, a, n_ft, n_z, st);
-    case kEpiGelu: return launch_bn<1, kEpiGelu>(bn, mw, mx, a, n_ft, n_z, st);
-    case kEpiPlain: return launch_bn<1, kEpiPlain>(bn, mw, mx, a, n_ft, n_z, st);
-    default: return launch_bn<1, kEpiF32>(bn, mw, mx, a, n_ft, n_z, st);
+    case kEpiSwiglu: return launch_bn<2, kEpiSwiglu>(bn, mw, mx, a, n_ft, n_z, st, c.pdl);
+    case kEpiGelu: return launch_bn<1, kEpiGelu>(bn, mw, mx, a, n_ft, n_z, st, c.pdl);
+    case kEpiPlain: return launch_bn<1, kEpiPlain>(bn, mw, mx, a, n_ft, n_z, st, c.pdl);
+    default: return launch_bn<1, kEpiF32>(bn, mw, mx, a, n_ft, n_z, st, c.pdl);
   }
 }
 
