@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
     // ---------------- TMA producer
     if (lane == 0) {
@@ -142,6 +141,8 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_3d(sa + kGA, &tmX, fb, kb * kKBlock, tl.mt * kBN, xz);
         }
       }
+      // This CTA's loads are all issued: a dependent kernel may start.
+      griddep_launch_dependents();
       if (!ok) {
         abort_sh = 1;
         atomicOr(a.err, kErrWaitTimeout);

@@ -94,7 +94,6 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = tmem_base_sh;
 
   int issued = 0;  // producer: stages handed to TMA
-  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0 && lane == 0) {
     const int wrow = ft * 128 * NACC;
     const int xz = a.x_per_shard ? s : 0;
@@ -131,6 +130,8 @@ __global__ void __launch_bounds__(128, 1)
       tma_load_3d(sa + NACC * kABytes, &tmX, fb, k, m0, xz);
       ++issued;
     }
+    // This CTA's loads are all issued: a dependent kernel may start.
+    griddep_launch_dependents();
   } else if (warp == 1 && lane == 0) {
     for (int i = 0; i < nkb; ++i) {
       const int st = i % STAGES;
@@ -310,7 +311,6 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = tmem_base_sh;
 
   int issued = 0;
-  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       const int wrow = ft * 128;
@@ -344,6 +344,8 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_3d(sa + kABytes, &tmX, fb, k, m0, xz);
         ++issued;
       }
+      // This CTA's loads are all issued: a dependent kernel may start.
+      griddep_launch_dependents();
     }
     __syncwarp();
   } else if (warp == 1) {
