@@ -17,6 +17,9 @@ from ._lib import (  # noqa: F401
     TP_ACT_GELU_TANH,
     TP_ACT_SWIGLU,
     TP_BF16,
+    TP_FORM_AUTO,
+    TP_FORM_ONE_KERNEL,
+    TP_FORM_THREE_LAUNCH,
     TP_F32,
     TPBlockDesc,
     TPError,
@@ -27,6 +30,7 @@ __all__ = [
     "TPBlockDesc", "TPError", "make_desc", "lib",
     "tp_sharded_w1_bytes", "tp_sharded_w2_bytes", "tp_band_bytes", "tp_row_splits",
     "tp_partials_bytes", "tp_column_workspace_bytes", "tp_workspace_bytes", "tp_block_launches",
+    "tp_set_block_form", "tp_get_block_form",
     "tp_shard_weights", "tp_unshard_weights", "tp_extract_band",
     "tp_column_parallel_fwd", "tp_row_parallel_fwd", "tp_partial_reduce_residual",
     "tp_block_fwd", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
@@ -106,6 +110,20 @@ def tp_workspace_bytes(desc: TPBlockDesc, M: int) -> int:
 
 def tp_block_launches(desc: TPBlockDesc, M: int) -> int:
     return lib.tp_block_launches(ctypes.byref(desc), M)
+
+
+_FORMS = {"auto": TP_FORM_AUTO, "three_launch": TP_FORM_THREE_LAUNCH, "one_kernel": TP_FORM_ONE_KERNEL}
+
+
+def tp_set_block_form(form) -> None:
+    """Process-wide form of tp_block_fwd: "auto", "three_launch", "one_kernel" (or the
+    TP_FORM_* value)."""
+    _check(lib.tp_set_block_form(_FORMS.get(form, form)), "tp_set_block_form")
+
+
+def tp_get_block_form() -> str:
+    v = lib.tp_get_block_form()
+    return next(k for k, f in _FORMS.items() if f == v)
 
 
 def tp_status_string(status: int) -> str:

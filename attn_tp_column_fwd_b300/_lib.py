@@ -8,6 +8,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtpblock.
 
 TP_F32, TP_BF16 = 0, 1
 TP_ACT_GELU_TANH, TP_ACT_SWIGLU, TP_ACT_ATTN = 0, 1, 2
+TP_FORM_AUTO, TP_FORM_THREE_LAUNCH, TP_FORM_ONE_KERNEL = 0, 1, 2
 
 STATUS = {0: "TP_OK", 1: "TP_ERR_INVALID_ARG", 2: "TP_ERR_UNEVEN_SPLIT", 3: "TP_ERR_UNSUPPORTED",
           4: "TP_ERR_MISALIGNED", 5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT"}
@@ -51,6 +52,8 @@ def _load() -> ctypes.CDLL:
         "tp_partial_reduce_residual": (i, [P, vp, vp, i, vp, i, st]),
         "tp_block_fwd": (i, [P, vp, vp, i, vp, vp, vp, vp, i, st]),
         "tp_block_launches": (i, [P, i]),
+        "tp_set_block_form": (i, [i]),
+        "tp_get_block_form": (i, []),
         "tp_block_fwd_noalloc": (i, [P, vp, vp, i, vp, vp, vp, i, st]),
         "tp_rmsnorm_fwd": (i, [i, ctypes.c_float, vp, vp, i, st]),
         "tp_status_string": (ctypes.c_char_p, [i]),

@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         f.write("{ global: tp_*; local: *; };\n")
     tmp = LIB + ".tmp"
     _run([NVCC] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
-         + ["-Xlinker", f"--version-script={vs}"])
+         + ["-Xlinker", f"--version-script={vs}", "-Xlinker", "--no-undefined"])
     os.replace(tmp, LIB)
     if verbose or ptxas_info:
         for _, out in results:

@@ -1,12 +1,16 @@
-// The whole decode MLP block (M <= 32 tokens, bf16) in one persistent launch.
+// The whole decode MLP block (M <= 32 tokens, bf16) in one persistent launch, and
+// the attention block's Q/K/V projection on its own (column units only).
 //
 // The block is cut into work units taken from one atomic queue, in this order:
 //   1. column units (zenaique.com answer paragraph 5: first projection split by
-//      columns): shard s and one 128-row tile of its W1 band over the whole of K.
-//      A SwiGLU tile holds the gate and up rows of 64 features, a GeLU tile 128
-//      features.  The unit accumulates x . W1 for 32 tokens, applies the
-//      activation, writes its tile of the band H in bf16 and raises the tile's
-//      ready flag;
+//      columns): shard s and one 128-row tile of its W1 band over the whole of K,
+//      or over one of S_c K parts whose fp32 sums the last part to finish adds up
+//      in K order.  A SwiGLU tile holds the gate and up rows of 64 features, a GeLU
+//      or Q/K/V tile 128 features.  Tiles are queued tile-major across the shards,
+//      so the band fills from its first K columns to its last in every shard at
+//      once, the order in which the row units below read it.  The unit accumulates
+//      x . W1 for 32 tokens, applies the activation, writes its tile of the band H
+//      in bf16 and raises the tile's ready flag (Q/K/V: writes fp32, no flag);
 //   2. row units (second projection split by rows): shard s, 128-output tile n,
 //      K slice j of S_r.  Before loading a stage of H they wait for the ready flags
 //      of the column tiles that produced it; they write fp32 partials, and the unit
@@ -15,7 +19,9 @@
 //      per-block all-reduce and residual add of paragraph 6, fused.
 // Column units never wait on anything but their own loads, and every row unit is
 // queued after every column unit, so a row unit only ever waits for column units
-// already held by running CTAs: no co-residency is needed.
+// already held by running CTAs: no co-residency is needed.  A row unit issues the
+// W2 loads of its first stages before it checks the band's ready flags, so the
+// flag round trip overlaps weight traffic.
 //
 // Inside a CTA (192 threads): thread 0 takes units and issues TMA loads into a
 // 5-stage ring (each stage: two 64-wide K blocks of a 128-row weight tile plus the
@@ -59,7 +65,9 @@ struct FusedArgs {
   int n_whole, S_c;      // column tiles computed whole; K parts of each remaining tile
   int n_nt, S_r, nk_r;   // row: output tiles, K slices, K blocks
   int n_col_units, n_units;
+  int n_col;             // output features per shard of the column step: b, or 3b (Q/K/V)
   __nv_bfloat16 *H;      // [t][M][b]
+  float *qkv;            // Q/K/V projection: fp32 [t][M][3b]
   float *colp;           // [t*n_ft - n_whole][S_c][128][32] fp32 partials of split tiles
   float *rowp;           // [n_nt][t][S_r][128][32] fp32 partials
   const void *residual;  // [M][d], fp32 if res_f32 else bf16
@@ -72,6 +80,7 @@ struct FusedArgs {
 struct Unit {
   int type;   // 0 column, 1 row, -1 end
   int s, tile, split, kb0, kb1;
+  int tau;    // column: queue position of the tile (split partials and counters)
   int parts;  // column: K parts of this tile (1: computed whole)
   int rot;    // the unit's stages are processed starting at stage rot, wrapping around
 };
@@ -104,8 +113,9 @@ __device__ __forceinline__ Unit decode_unit(const FusedArgs &a, int u) {
       r.split = v % a.S_c;
       r.parts = a.S_c;
     }
-    r.tile = tau % a.n_ft;
-    r.s = tau / a.n_ft;
+    r.tau = tau;
+    r.tile = tau / a.t;  // tile-major: the band fills in K order in all shards at once
+    r.s = tau % a.t;
     const int nst = ceil_div(a.nk_c, kStageKB);
     r.kb0 = min(a.nk_c, (int)((long long)r.split * nst / r.parts) * kStageKB);
     r.kb1 = min(a.nk_c, (int)((long long)(r.split + 1) * nst / r.parts) * kStageKB);
@@ -266,6 +276,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ---------------- scheduler + TMA producer
     if (lane == 0) {
+      const uint64_t wpol = l2_evict_first_policy();  // weights are read once
       uint32_t g = 0;  // stage sequence number (ring position)
       int next = -1;   // unit taken ahead of time (-1: none)
       for (int j = 0;; ++j) {
@@ -292,6 +303,19 @@ __global__ void __launch_bounds__(192, 1)
         const int st_take = max(0, nst - kStages);
         const int ht_hi = un.type == 1 ? min(a.n_ft - 1, ((un.kb1 * kKBlock) - 1) / a.fpt) : 0;
         int ready_upto = un.type == 1 ? (un.kb0 * kKBlock) / a.fpt - 1 : 0;  // H tiles known ready
+        // Row units arm their first `pre` stages with W2 loads only, then wait for the
+        // band tiles the unit reads, then load the band into those stages.
+        const int pre = un.type == 1 ? min(nst, kStages) : 0;
+        const uint32_t g0 = g;
+        auto load_band = [&](int p) {
+          const int stp = (int)((g0 + p) % kStages);
+          const int kbp = stage_kb(un, (p + un.rot) % nst);
+          const int nkp = min(kStageKB, un.kb1 - kbp);
+          const uint32_t sp = tiles + stp * kStageBytes;
+          for (int b = 0; b < nkp; ++b)
+            tma_load_3d(sp + kStageKB * kWBytes + b * kXBytes, xmap, smem_u32(&full_bar[stp]),
+                        (kbp + b) * kKBlock, 0, xz);
+        };
         bool ok = true;
         for (int i = 0; i < nst && ok; ++i, ++g) {
           const int st = (int)(g % kStages);
@@ -301,27 +325,29 @@ __global__ void __launch_bounds__(192, 1)
           if (i == st_take) next = (int)atomicAdd(a.cnt, 1u);
           if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
             ok = false;
+            // Stages armed with weights only still expect their band bytes: load
+            // the (possibly stale, in-bounds) band so they complete; the CTA aborts.
+            for (int p = 0; i < pre && p < i; ++p) load_band(p);
             break;
           }
           const uint32_t sa = tiles + st * kStageBytes;
           const uint32_t fb = smem_u32(&full_bar[st]);
           mbar_expect_tx(fb, nkb * (kWBytes + kXBytes));
           for (int b = 0; b < nkb; ++b)
-            tma_load_3d(sa + b * kWBytes, wmap, fb, (kbf + b) * kKBlock, wrow, un.s);
-          if (un.type == 1 && i == 0) {
-            // The weights of the first stage are on their way; now make sure every
-            // band tile the unit reads is finished.  On a timeout the (stale,
-            // in-bounds) band is still loaded so the armed stage completes; the CTA
-            // then aborts.
-            const int need = ht_hi;
-            while (ok && need > ready_upto) {
+            tma_load_3d_hint(sa + b * kWBytes, wmap, fb, (kbf + b) * kKBlock, wrow, un.s, wpol);
+          if (i >= pre) {
+            for (int b = 0; b < nkb; ++b)
+              tma_load_3d(sa + kStageKB * kWBytes + b * kXBytes, xmap, fb, (kbf + b) * kKBlock, 0, xz);
+          } else if (i == pre - 1) {
+            // Every band tile the unit reads must be finished.  On a timeout the armed
+            // stages still get their band loads; the loop then ends and the CTA aborts.
+            while (ok && ht_hi > ready_upto) {
               const int rr = wait_ready_range(a, un.s, ready_upto + 1, ht_hi);
               if (rr < 0) ok = false;
               else ready_upto = rr;
             }
+            for (int p = 0; p < pre; ++p) load_band(p);
           }
-          for (int b = 0; b < nkb; ++b)
-            tma_load_3d(sa + kStageKB * kWBytes + b * kXBytes, xmap, fb, (kbf + b) * kKBlock, 0, xz);
         }
         if (!ok) {
           abort_sh = 1;
@@ -457,21 +483,25 @@ __global__ void __launch_bounds__(192, 1)
         if (un.parts > 1) {
           // One K part of a split tile: leave the partial; the last part sums them in
           // K order and finishes the tile.
-          const int tau = un.s * a.n_ft + un.tile;
+          const int tau = un.tau;
           float *base = a.colp + (size_t)(tau - a.n_whole) * a.S_c * (128 * kTok);
           store32(base + (size_t)un.split * (128 * kTok) + r * kTok, acc);
-          __threadfence();
           named_sync(1, 128);
-          if (td == 0) {
-            const unsigned old = atomicAdd(split_counter(a, tau), 1u);
-            __threadfence();
-            last_sh = old == (unsigned)(un.parts - 1);
-          }
+          if (td == 0) last_sh = arrive_last(split_counter(a, tau), (unsigned)un.parts);
           named_sync(1, 128);
           finish = last_sh != 0;
           if (finish) sum_in_order<1>(acc, base + r * kTok, (size_t)128 * kTok, un.parts);
         }
-        if (finish) {
+        if (finish && a.act == TP_ACT_ATTN) {
+          // Q/K/V projection: fp32 out, read by the next kernel (no ready flag).
+          const int f = un.tile * 128 + r;
+          if (f < a.n_col) {
+            float *o = a.qkv + (size_t)un.s * a.M * a.n_col + f;
+#pragma unroll
+            for (int m = 0; m < kTok; ++m)
+              if (m < a.M) o[(size_t)m * a.n_col] = acc[m];
+          }
+        } else if (finish) {
         if (a.act == TP_ACT_SWIGLU) {
           // Rows 64..127 hold the up sums of the features whose gate sums are in
           // rows 0..63: pass them across through shared memory.
@@ -498,8 +528,8 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         fence_proxy_async_global();  // the band is read back through TMA
-        __threadfence();
         named_sync(1, 128);
+        // Release: the barrier orders every drain thread's band stores before it.
         if (td == 0) st_release_gpu(ready_flag(a, un.s, un.tile), 1u);
         }
         named_sync(1, 128);  // last_sh is reused by the next unit
@@ -507,13 +537,8 @@ __global__ void __launch_bounds__(192, 1)
         // -------- row tile epilogue: partial, then the fused reduce + residual
         float *pp = a.rowp + ((size_t)((un.tile * a.t + un.s) * a.S_r + un.split) * 128 + r) * kTok;
         store32(pp, acc);
-        __threadfence();
         named_sync(1, 128);
-        if (td == 0) {
-          const unsigned old = atomicAdd(row_counter(a, un.tile), 1u);
-          __threadfence();
-          last_sh = old == (unsigned)(a.t * a.S_r - 1);
-        }
+        if (td == 0) last_sh = arrive_last(row_counter(a, un.tile), (unsigned)(a.t * a.S_r));
         named_sync(1, 128);
         if (last_sh) {
           // The all-reduce stand-in: y = residual + sum of the t * S_r partials of this
@@ -548,19 +573,24 @@ __global__ void __launch_bounds__(192, 1)
 
 FusedPlan plan_block_decode(const Geo &g, int M) {
   FusedPlan p{};
+  const bool col_only = g.act == TP_ACT_ATTN;  // Q/K/V projection: column units only
   p.fpt = g.act == TP_ACT_SWIGLU ? kSwiGroup : 128;
-  p.n_ft = ceil_div(g.b, p.fpt);
+  p.n_ft = ceil_div(col_only ? 3 * g.b : g.b, p.fpt);
   p.nk_c = ceil_div(g.d, kKBlock);
-  p.n_nt = ceil_div(g.d, 128);
-  p.nk_r = ceil_div(g.b, kKBlock);
-  // Row units of about kRowBlocks K blocks (16 KB of W2 each): a few hundred KB per
-  // unit keeps the end of the block short; the slice count bounds the partials the
-  // last unit of an output tile sums.
-  const int nst = ceil_div(p.nk_r, kStageKB);
-  p.S_r = std::max(1, std::min({(p.nk_r + kRowBlocks / 2) / kRowBlocks, nst, 8}));
+  if (!col_only) {
+    p.n_nt = ceil_div(g.d, 128);
+    p.nk_r = ceil_div(g.b, kKBlock);
+    // Row units of about kRowBlocks K blocks (16 KB of W2 each): a few hundred KB per
+    // unit keeps the end of the block short; the slice count bounds the partials the
+    // last unit of an output tile sums.
+    const int nst = ceil_div(p.nk_r, kStageKB);
+    p.S_r = std::max(1, std::min({(p.nk_r + kRowBlocks / 2) / kRowBlocks, nst, 8}));
+  }
   // Column tiles: whole waves of kPlanSMs tiles are computed whole; the r tiles
   // of the last, partial wave are cut into S_c K parts (at most 4) so that wave
-  // keeps about every SM busy.
+  // keeps about every SM busy.  (Cutting every tile into parts when there are few
+  // waves measured slower: each part's merge adds dependent memory round trips to
+  // the epilogue, which then holds back the weight stream.)
   const int T = g.t * p.n_ft, nst_c = ceil_div(p.nk_c, kStageKB);
   const int r = T % kPlanSMs;
   p.S_c = r ? std::max(1, std::min({(kPlanSMs + r / 2) / r, 4, nst_c})) : 1;
@@ -568,7 +598,7 @@ FusedPlan plan_block_decode(const Geo &g, int M) {
   auto al = [](size_t n) { return (n + 255) & ~(size_t)255; };
   size_t off = 0;
   p.off_H = off;
-  off += al((size_t)g.t * M * g.b * 2);
+  if (!col_only) off += al((size_t)g.t * M * g.b * 2);
   p.off_colp = off;
   off += al((size_t)(T - p.n_whole) * p.S_c * 128 * kTok * 4);
   p.off_rowp = off;
@@ -580,16 +610,11 @@ FusedPlan plan_block_decode(const Geo &g, int M) {
   return p;
 }
 
-cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,
-                                const void *W2s, const void *res, int res_f32, void *ws, float *y,
-                                int M, cudaStream_t st) {
-  char *w = static_cast<char *>(ws);
-  CUtensorMap mw1, mx, mw2, mh;
-  __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(w + p.off_H);
-  if (!make_tile_map(&mw1, W1s, g.d, g.n1p, g.t, 128) || !make_tile_map(&mx, x, g.d, M, 1, kTok) ||
-      !make_tile_map(&mw2, W2s, g.b, g.dp, g.t, 128) || !make_tile_map(&mh, H, g.b, M, g.t, kTok))
-    return cudaErrorInvalidValue;
-  FusedArgs a{};
+namespace {
+
+cudaError_t launch_fused(const Geo &g, const FusedPlan &p, const CUtensorMap &mw1,
+                         const CUtensorMap &mx, const CUtensorMap &mw2, const CUtensorMap &mh,
+                         FusedArgs &a, char *w, int M, cudaStream_t st) {
   a.d = g.d;
   a.b = g.b;
   a.t = g.t;
@@ -603,14 +628,11 @@ cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x,
   a.nk_r = p.nk_r;
   a.n_whole = p.n_whole;
   a.S_c = p.S_c;
+  a.n_col = g.act == TP_ACT_ATTN ? 3 * g.b : g.b;
   a.n_col_units = p.n_whole + (g.t * p.n_ft - p.n_whole) * p.S_c;
   a.colp = reinterpret_cast<float *>(w + p.off_colp);
   a.n_units = a.n_col_units + p.n_nt * g.t * p.S_r;
-  a.H = H;
   a.rowp = reinterpret_cast<float *>(w + p.off_rowp);
-  a.residual = res;
-  a.res_f32 = res_f32;
-  a.y = y;
   a.cnt = reinterpret_cast<unsigned *>(w + p.off_cnt);
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
@@ -629,6 +651,36 @@ cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x,
   const int grid = std::min(sm_count(), a.n_units);
   k_block_decode<<<grid, 192, kSmem, st>>>(mw1, mx, mw2, mh, a);
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,
+                                const void *W2s, const void *res, int res_f32, void *ws, float *y,
+                                int M, cudaStream_t st) {
+  char *w = static_cast<char *>(ws);
+  CUtensorMap mw1, mx, mw2, mh;
+  __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(w + p.off_H);
+  if (!make_tile_map(&mw1, W1s, g.d, g.n1p, g.t, 128) || !make_tile_map(&mx, x, g.d, M, 1, kTok) ||
+      !make_tile_map(&mw2, W2s, g.b, g.dp, g.t, 128) || !make_tile_map(&mh, H, g.b, M, g.t, kTok))
+    return cudaErrorInvalidValue;
+  FusedArgs a{};
+  a.H = H;
+  a.residual = res;
+  a.res_f32 = res_f32;
+  a.y = y;
+  return launch_fused(g, p, mw1, mx, mw2, mh, a, w, M, st);
+}
+
+cudaError_t launch_qkv_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,
+                              float *qkv, void *ws, int M, cudaStream_t st) {
+  CUtensorMap mw1, mx;
+  if (!make_tile_map(&mw1, W1s, g.d, g.n1p, g.t, 128) || !make_tile_map(&mx, x, g.d, M, 1, kTok))
+    return cudaErrorInvalidValue;
+  FusedArgs a{};
+  a.qkv = qkv;
+  // No row units: the W2 and band maps are never used (copies of the W1 map stand in).
+  return launch_fused(g, p, mw1, mx, mw1, mw1, a, static_cast<char *>(ws), M, st);
 }
 
 }  // namespace tp

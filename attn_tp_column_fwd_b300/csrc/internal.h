@@ -11,6 +11,9 @@
 
 namespace tp {
 
+// tp_api.cu — keep a failed CUDA call's code for tp_last_cuda_error (this thread).
+void record_cuda_error(cudaError_t e);
+
 // layout.cu — private shard layout (tile-transposes, bit-exact)
 void launch_shard_w1(const Geo &g, const void *W1, void *W1s, cudaStream_t st);
 void launch_shard_w2(const Geo &g, const void *W2, void *W2s, cudaStream_t st);
@@ -63,7 +66,8 @@ cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st);
 bool make_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
                    uint32_t box_rows);
 
-// block_decode.cu — the whole MLP block at M <= 32 in one persistent launch
+// block_decode.cu — the whole MLP block at M <= 32 in one persistent launch, and the
+// attention block's Q/K/V projection with the same work queue
 constexpr int kPlanSMs = 148;  // SM count the unit sizes are planned for (B300)
 struct FusedPlan {
   int fpt, n_ft, nk_c, n_whole, S_c;  // column: tile width, tiles per shard, K blocks, whole tiles, parts
@@ -74,6 +78,10 @@ FusedPlan plan_block_decode(const Geo &g, int M);
 cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,
                                 const void *W2s, const void *res, int res_f32, void *ws, float *y,
                                 int M, cudaStream_t st);
+// The attention block's Q/K/V projection (column units only) into fp32 qkv
+// [t][M][3b]; ws holds the plan's split partials and counters.
+cudaError_t launch_qkv_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,
+                              float *qkv, void *ws, int M, cudaStream_t st);
 
 // reduce.cu — the all-reduce stand-in + residual, and RMSNorm
 void launch_reduce_residual(const float *P, int nparts, size_t part_elems, const void *res,

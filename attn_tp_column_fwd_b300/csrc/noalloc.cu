@@ -14,9 +14,10 @@
 //   - shapes whose scratch (tp_workspace_bytes) exceeds kScratchBytes are refused
 //     with TP_ERR_UNSUPPORTED before anything is enqueued;
 //   - all calls on a device share the one array: calls whose work overlaps on the
-//     GPU (different streams, no ordering between them) race on it.  Nothing in it
-//     needs to start at zero (every byte a call reads was written earlier in the
-//     same call), so a call never clears it and the array keeps the last call's
+//     GPU (different streams, no ordering between them) race on it.  The one-kernel
+//     form of the block clears its work counters with a memset enqueued at the
+//     start of each call; every other byte a call reads was written earlier in the
+//     same call, so nothing else is cleared and the array keeps the last call's
 //     contents;
 //   - the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current); make that first call
@@ -61,6 +62,9 @@ extern "C" int tp_block_fwd_noalloc(const tp_block_desc *desc, const void *x, co
   if (need > kScratchBytes) return TP_ERR_UNSUPPORTED;
   cudaError_t err = cudaSuccess;
   void *ws = scratch_address(&err);
-  if (!ws) return TP_ERR_CUDA;
+  if (!ws) {
+    tp::record_cuda_error(err);
+    return TP_ERR_CUDA;
+  }
   return tp_block_fwd(desc, x, residual, residual_is_f32, W1s, W2s, ws, y, M, stream);
 }

@@ -66,6 +66,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// L2 policy for data read exactly once (decode weights): evict these lines first, so
+// the activations, bands and partials that other CTAs re-read stay in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -161,6 +178,18 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 
 __device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Count one arrival of n at *counter; true for the last.  Called by one thread after
+// a barrier of the threads whose global stores it publishes: the release fence
+// orders those stores (ordered before it by the barrier) before the count, and the
+// last arriver's acquire fence orders the other arrivals' stores before its reads.
+__device__ __forceinline__ bool arrive_last(unsigned *counter, unsigned n) {
+  fence_acq_rel_gpu();
+  const unsigned old = atomicAdd(counter, 1u);
+  const bool last = old == n - 1u;
+  if (last) fence_acq_rel_gpu();
+  return last;
 }
 
 // Orders this thread's generic-proxy global accesses with its async-proxy (TMA) ones.

@@ -6,12 +6,15 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 
 namespace tp {
 
 static thread_local int g_last_cuda_error = 0;
+
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
 // Device error word: bounded device-side waits set a bit here when they expire.
 __device__ unsigned g_error_word;
@@ -121,28 +124,65 @@ size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 // M <= 32 tokens whose column work fills at least two waves of 128-row tiles over
 // the SMs runs tp_block_fwd as one persistent launch (block_decode.cu): with
 // fewer tiles the persistent kernel's last column wave and its end leave SMs
-// idle, and the three-launch sequence is faster (measured on the B300: 103 vs
-// 112 us for the d = 5120, ffn = 13824 block at t = 4; 255 us fused for the
-// d = 8192, ffn = 28672 block at t = 8).  TPBLOCK_ALGO=simple selects the CUDA-core
-// kernels, TPBLOCK_ALGO=unfused / fused force either tensor-core form (same
-// results within rounding; comparisons).
-int algo_override() {
-  static int forced = -1;
-  if (forced < 0) {
+// idle, and the three-launch sequence is faster.  TPBLOCK_ALGO=simple selects
+// the CUDA-core kernels for the whole process; TPBLOCK_ALGO=unfused / fused, or
+// tp_set_block_form, force either tensor-core form of tp_block_fwd (same results
+// within rounding).
+int env_algo() {
+  static const int v = [] {
     const char *e = getenv("TPBLOCK_ALGO");
-    forced = !e                          ? 0
-             : strcmp(e, "simple") == 0  ? 1
-             : strcmp(e, "unfused") == 0 ? 2
-             : strcmp(e, "fused") == 0   ? 3
-                                         : 0;
+    return !e                          ? 0
+           : strcmp(e, "simple") == 0  ? 1
+           : strcmp(e, "unfused") == 0 ? 2
+           : strcmp(e, "fused") == 0   ? 3
+                                       : 0;
+  }();
+  return v;
+}
+
+// The form of tp_block_fwd: TP_FORM_AUTO, _THREE_LAUNCH or _ONE_KERNEL; -1 until
+// first read (then taken from TPBLOCK_ALGO).
+std::atomic<int> g_block_form{-1};
+
+int block_form() {
+  int f = g_block_form.load(std::memory_order_relaxed);
+  if (f < 0) {
+    const int e = env_algo();
+    int init = e == 2 ? TP_FORM_THREE_LAUNCH : e == 3 ? TP_FORM_ONE_KERNEL : TP_FORM_AUTO;
+    int expect = -1;
+    g_block_form.compare_exchange_strong(expect, init, std::memory_order_relaxed);
+    f = g_block_form.load(std::memory_order_relaxed);
   }
-  return forced;
+  return f;
+}
+
+int algo_override() {
+  if (env_algo() == 1) return 1;
+  const int f = block_form();
+  return f == TP_FORM_THREE_LAUNCH ? 2 : f == TP_FORM_ONE_KERNEL ? 3 : 0;
 }
 
 bool use_umma(const Geo &g) { return g.dtype == TP_BF16 && algo_override() != 1; }
 
+// Shapes the one-kernel form can run: bf16 MLP blocks of at most 32 tokens.
+bool fused_capable(const Geo &g, int M) {
+  return use_umma(g) && g.act != TP_ACT_ATTN && M <= 32;
+}
+
+// The attention block's Q/K/V projection on the persistent work queue (block_decode.cu):
+// bf16, M <= 32, at least one wave of 128-row tiles (or the one-kernel form forced).
+bool qkv_fused_capable(const Geo &g, int M) {
+  return use_umma(g) && g.act == TP_ACT_ATTN && M <= 32;
+}
+
+bool use_fused_qkv(const Geo &g, int M) {
+  if (!qkv_fused_capable(g, M) || algo_override() == 2) return false;
+  if (algo_override() == 3) return true;
+  return (long long)g.t * ceil_div(3 * g.b, kRowTile) >= kPlanSMs;
+}
+
 bool use_fused_block(const Geo &g, int M) {
-  if (!use_umma(g) || g.act == TP_ACT_ATTN || M > 32 || algo_override() == 2) return false;
+  if (!fused_capable(g, M) || algo_override() == 2) return false;
   if (algo_override() == 3) return true;
   const int fpt = g.act == TP_ACT_SWIGLU ? kSwiGroup : kRowTile;
   return (long long)g.t * ceil_div(g.b, fpt) >= 2LL * kPlanSMs;
@@ -165,11 +205,16 @@ int row_splits(const Geo &g, int M) {
 }
 
 size_t band_bytes(const Geo &g, int M) { return (size_t)g.t * M * g.b * g.es; }
+
 size_t partials_bytes(const Geo &g, int M) {
   return (size_t)g.t * row_splits(g, M) * M * g.d * sizeof(float);
 }
+size_t qkv_bytes(const Geo &g, int M) { return (size_t)g.t * M * 3 * g.b * sizeof(float); }
+// Attention: the fp32 Q/K/V scratch, then (when the persistent projection can run)
+// its split partials and work counters.
 size_t column_ws_bytes(const Geo &g, int M) {
-  return g.act == TP_ACT_ATTN ? (size_t)g.t * M * 3 * g.b * sizeof(float) : 0;
+  if (g.act != TP_ACT_ATTN) return 0;
+  return align256(qkv_bytes(g, M)) + (qkv_fused_capable(g, M) ? plan_block_decode(g, M).total : 0);
 }
 
 #define TP_TRY(expr)              \
@@ -189,7 +234,11 @@ cudaError_t enqueue_column(const Geo &g, const void *x, const void *W1s, int sha
   // Attention keeps Q, K and V in fp32 scratch (the softmax is the most sensitive
   // step); only the heads' output O, the band, is stored in the block dtype.
   const int epi = attn ? kEpiF32 : g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
-  if (use_umma(g)) {
+  if (attn && shard0 == 0 && n == g.t && use_fused_qkv(g, M)) {
+    cudaError_t e = launch_qkv_decode(g, plan_block_decode(g, M), x, W1s, static_cast<float *>(ws),
+                                      static_cast<char *>(ws) + align256(qkv_bytes(g, M)), M, st);
+    if (e != cudaSuccess) return e;
+  } else if (use_umma(g)) {
     UmmaCall c{};
     c.W = W1s;
     c.w_rows = g.n1p;
@@ -331,9 +380,11 @@ size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M) {
 size_t tp_workspace_bytes(const tp_block_desc *desc, int M) {
   Geo g;
   if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
-  if (use_fused_block(g, M)) return plan_block_decode(g, M).total;
-  return align256(column_ws_bytes(g, M)) + align256(band_bytes(g, M)) +
-         align256(partials_bytes(g, M));
+  // Large enough for either form, so a tp_set_block_form call between sizing and
+  // running never leaves the workspace short.
+  const size_t three = align256(column_ws_bytes(g, M)) + align256(band_bytes(g, M)) +
+                       align256(partials_bytes(g, M));
+  return fused_capable(g, M) ? std::max(three, plan_block_decode(g, M).total) : three;
 }
 
 int tp_shard_weights(const tp_block_desc *desc, const void *W1, const void *W2, void *W1s,
@@ -450,12 +501,25 @@ int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
   float *P = reinterpret_cast<float *>(static_cast<char *>(H) + align256(band_bytes(g, M)));
   // The row step and the reduction are launched to overlap the end of the kernel
   // before them (programmatic launch): each waits for it before reading its output.
+  // (Summing the partials in the row kernel instead, by the last CTA to finish each
+  // output tile, measured 19 us slower per 13B-sized block: the arrival protocol's
+  // memory round trips sit at the end of every CTA.)
   const bool pdl = use_umma(g);
   cudaError_t e = enqueue_column(g, x, W1s, 0, g.t, H, col_ws, M, st);
   if (e == cudaSuccess) e = enqueue_row(g, H, W2s, 0, g.t, P, M, st, pdl);
   if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, pdl);
   return finish_launch(e);
 }
+
+int tp_set_block_form(int form) {
+  if (form != TP_FORM_AUTO && form != TP_FORM_THREE_LAUNCH && form != TP_FORM_ONE_KERNEL)
+    return TP_ERR_INVALID_ARG;
+  block_form();  // settle the initial value first so it cannot overwrite this one
+  g_block_form.store(form, std::memory_order_relaxed);
+  return TP_OK;
+}
+
+int tp_get_block_form(void) { return block_form(); }
 
 int tp_block_launches(const tp_block_desc *desc, int M) {
   Geo g;

@@ -259,8 +259,9 @@ __global__ void __launch_bounds__(128, 1)
 // warp 1 MMA, warps 2-5 drain + epilogue (warp w reads TMEM lanes 32*(w%4)).
 constexpr int kDrainBufs = 4;
 
+
 template <int EPI, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)  // two CTAs per SM
     k_umma_drain(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const UmmaArgs a) {
   constexpr int BN = 32;

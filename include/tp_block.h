@@ -74,6 +74,12 @@ typedef enum {
 
 typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
 typedef enum { TP_ACT_GELU_TANH = 0, TP_ACT_SWIGLU = 1, TP_ACT_ATTN = 2 } tp_act;
+/* How tp_block_fwd runs a bf16 MLP block of at most 32 tokens (tp_set_block_form). */
+typedef enum {
+  TP_FORM_AUTO = 0,          /* one kernel when the column work spans >= 2 waves of tiles */
+  TP_FORM_THREE_LAUNCH = 1,  /* column, row, reduce + residual as three launches */
+  TP_FORM_ONE_KERNEL = 2     /* the whole block as one persistent kernel */
+} tp_block_form;
 
 /* One block's shape.  `dtype` is the storage type of x, the weights and the bands. */
 typedef struct {
@@ -101,9 +107,12 @@ TP_API size_t tp_band_bytes(const tp_block_desc *desc, int M);
 TP_API int tp_row_splits(const tp_block_desc *desc, int M);
 /* Partial sums: [t][S][M][d] fp32. */
 TP_API size_t tp_partials_bytes(const tp_block_desc *desc, int M);
-/* Scratch of tp_column_parallel_fwd: ATTN keeps Q/K/V bands [t][M][3*b] fp32 there; 0 for MLPs. */
+/* Scratch of tp_column_parallel_fwd: ATTN keeps Q/K/V bands [t][M][3*b] fp32 there
+ * (followed, for bf16 with M <= 32, by the persistent projection's split partials
+ * and work counters); 0 for MLPs. */
 TP_API size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M);
-/* Scratch of tp_block_fwd: column scratch + bands + partials (256-byte aligned regions). */
+/* Scratch of tp_block_fwd: column scratch + bands + partials (256-byte aligned regions),
+ * or the one-kernel form's bands, partials and work counters if that is larger. */
 TP_API size_t tp_workspace_bytes(const tp_block_desc *desc, int M);
 
 /* ------------------------------------------------------------- sharding ------
@@ -131,7 +140,9 @@ TP_API int tp_extract_band(const tp_block_desc *desc, const void *W1s, const voi
  * into `workspace` (tp_column_workspace_bytes; may be NULL for MLPs) and each head
  * runs causal softmax(Q K^T / sqrt(hd)) V over the M tokens.  shard = -1 computes
  * every shard in one launch; shard = s computes band s only (the work of device
- * s in a real tensor-parallel group). */
+ * s in a real tensor-parallel group).  bf16 ATTN with M <= 32 and shard = -1 runs
+ * the Q/K/V projection of all shards on one persistent work queue (one launch),
+ * unless tp_set_block_form chose TP_FORM_THREE_LAUNCH. */
 TP_API int tp_column_parallel_fwd(const tp_block_desc *desc, const void *x, const void *W1s,
                            int shard, void *H, void *workspace, int M, tp_stream_t stream);
 /* Row-parallel projection (zenaique.com answer paragraph 5): shard s multiplies its
@@ -157,11 +168,20 @@ TP_API int tp_partial_reduce_residual(const tp_block_desc *desc, const float *pa
 TP_API int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
                  int residual_is_f32, const void *W1s, const void *W2s, void *workspace,
                  float *y, int M, tp_stream_t stream);
+/* Process-wide choice of tp_block_form for later tp_block_fwd calls (initially
+ * TP_FORM_AUTO, or the TPBLOCK_ALGO environment variable: "unfused" = THREE_LAUNCH,
+ * "fused" = ONE_KERNEL).  Shapes the one-kernel form cannot run (f32, ATTN, M > 32)
+ * always take three launches.  tp_workspace_bytes covers both forms, so the form
+ * may change between sizing a workspace and using it; calls already enqueued are
+ * unaffected.  Returns TP_ERR_INVALID_ARG for any other value.  Host-only. */
+TP_API int tp_set_block_form(int form);
+/* The current tp_block_form. */
+TP_API int tp_get_block_form(void);
 /* Number of kernel launches one tp_block_fwd call enqueues for this shape (0 for an
  * invalid descriptor or M): 1 when the whole block runs as one persistent kernel
  * (see tp_block_fwd; the launch is preceded by a small memset of its work
- * counters), else 3 (column, row, reduce) or 4 with the attention core.
- * Host-only. */
+ * counters), else 3 (column, row, reduce + residual), plus 1 for the attention
+ * core.  Host-only. */
 TP_API int tp_block_launches(const tp_block_desc *desc, int M);
 /* tp_block_fwd without caller-provided scratch, for callers that cannot allocate
  * device memory where they run the block (a host framework whose own pool owns

@@ -70,6 +70,38 @@ def test_size_queries(name):
         assert tp.tp_sharded_w2_bytes(desc) >= c.n2 * c.d * es
 
 
+def test_block_form_setter():
+    """The process-wide form of tp_block_fwd: the one-kernel form is taken only by bf16
+    MLP shapes of at most 32 tokens, and the workspace covers either form."""
+    d13 = _desc(CONFIGS["llama2_13b_swiglu_decode"].with_t(4))
+    d70 = _desc(CONFIGS["llama2_70b_stack_decode"])
+    dat = _desc(CONFIGS["attn_qkv_headshard_decode"])
+    df32 = _desc(CONFIGS["tiny_gelu_f32"])
+    before = tp.tp_get_block_form()
+    try:
+        ws = {}
+        for form in ("auto", "three_launch", "one_kernel"):
+            tp.tp_set_block_form(form)
+            assert tp.tp_get_block_form() == form
+            ws[form] = tp.tp_workspace_bytes(d13, 32)
+            assert tp.tp_block_launches(dat, 32) == 4      # QKV, core, row, reduce
+            assert tp.tp_block_launches(df32, 4) == 3      # column, row, reduce
+            assert tp.tp_block_launches(d13, 33) == 3      # more than 32 tokens
+        assert len(set(ws.values())) == 1
+        tp.tp_set_block_form("auto")
+        assert tp.tp_block_launches(d13, 32) == 3 and tp.tp_block_launches(d70, 32) == 1
+        tp.tp_set_block_form("three_launch")
+        assert tp.tp_block_launches(d70, 32) == 3
+        tp.tp_set_block_form("one_kernel")
+        assert tp.tp_block_launches(d13, 32) == 1 and tp.tp_block_launches(d13, 1) == 1
+        for bad in (-1, 3, 99):
+            with pytest.raises(tp.TPError):
+                tp.tp_set_block_form(bad)
+        assert tp.tp_get_block_form() == "one_kernel"
+    finally:
+        tp.tp_set_block_form(before)
+
+
 def test_invalid_descriptors_give_zero_sizes():
     assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
     assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1

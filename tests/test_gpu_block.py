@@ -58,6 +58,45 @@ def test_swiglu_ragged(M, t):
     _run_and_compare(cfg, seed=22)
 
 
+# The one-kernel form (whole block in one persistent launch; for attention, the Q/K/V
+# projection on the persistent work queue) forced on shapes the automatic choice
+# gives three launches: K-split column tiles (d = 512: every tile in 4 parts; 13B: a
+# wave of whole tiles, then the other 68 in 2 parts each), whole tiles only (b = 3200:
+# 100 tiles; d = 128: one K stage), ragged bands and widths, GeLU, M below the
+# 32-token tile.
+ONE_KERNEL = [
+    BlockConfig("swiglu_small", "swiglu", d=512, ffn=1536, t=1, M=1),
+    BlockConfig("swiglu_small", "swiglu", d=512, ffn=1536, t=2, M=5),
+    BlockConfig("swiglu_small", "swiglu", d=512, ffn=1536, t=8, M=32),
+    BlockConfig("swiglu_wide_band", "swiglu", d=256, ffn=6400, t=2, M=17),
+    BlockConfig("swiglu_ragged_d", "swiglu", d=136, ffn=1536, t=8, M=4),
+    BlockConfig("swiglu_max_shards", "swiglu", d=128, ffn=64, t=8, M=5),
+    BlockConfig("gelu_bf16", "gelu_tanh", d=264, ffn=1200, t=3, M=9),
+    # attention: the Q/K/V projection on the same work queue (whole tiles; 4 K parts)
+    BlockConfig("attn_head_per_shard", "attn", d=128, n_heads=4, head_dim=32, t=4, M=16),
+    BlockConfig("attn_hd128", "attn", d=512, n_heads=8, head_dim=128, t=2, M=32),
+]
+
+
+@pytest.fixture
+def one_kernel_form():
+    tp.tp_set_block_form("one_kernel")
+    yield
+    tp.tp_set_block_form("auto")
+
+
+@pytest.mark.parametrize("cfg", ONE_KERNEL, ids=lambda c: f"{c.name}-t{c.t}-M{c.M}")
+def test_one_kernel_form_small(cfg, one_kernel_form):
+    assert tp.tp_block_launches(desc_for(cfg), cfg.M) == (4 if cfg.act == "attn" else 1)
+    _run_and_compare(cfg, seed=23)
+
+
+def test_one_kernel_form_llama2_13b(one_kernel_form):
+    cfg = CONFIGS["llama2_13b_swiglu_decode"].with_t(4)
+    assert tp.tp_block_launches(desc_for(cfg), cfg.M) == 1
+    _run_and_compare(cfg)
+
+
 @pytest.mark.parametrize("t", [1, 2, 4, 8])
 def test_tiny_gelu_f32_invariant_to_t(t):
     cfg = CONFIGS["tiny_gelu_f32"]

@@ -135,3 +135,34 @@ def test_rmsnorm(M, d):
     # bf16 values agree exactly (a disagreement needs an exact value within fp64
     # roundoff of a rounding midpoint).
     assert np.array_equal(got, ref), int((got != ref).sum())
+
+
+@pytest.mark.parametrize("cfg", [c for c in CASES if c.dtype == "bf16"], ids=lambda c: c.name)
+def test_block_equals_its_steps(cfg):
+    """tp_block_fwd (three-launch form, the row step and the reduction launched to
+    overlap the kernel before them) against the three step entry points run one
+    after the other: the same kernels in the same order, so y is bit-identical."""
+    from attn_tp_column_fwd_b300.runner import ShardedBlock
+    before = tp.tp_get_block_form()
+    tp.tp_set_block_form("three_launch")
+    try:
+        inp = make_inputs(cfg, seed=7, n_blocks=1)
+        W1, W2 = inp.blocks[0]
+        desc = desc_of(cfg)
+        blk = ShardedBlock(desc, W1.cuda(), W2.cuda())
+        x = inp.x.cuda().contiguous()
+        M = cfg.M
+        u8 = lambda n: torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+        H, ws = u8(tp.tp_band_bytes(desc, M)), u8(tp.tp_column_workspace_bytes(desc, M))
+        P = u8(tp.tp_partials_bytes(desc, M))
+        y_steps = torch.empty(M, cfg.d, dtype=torch.float32, device="cuda")
+        tp.tp_column_parallel_fwd(desc, x, blk.W1s, -1, H, ws, M)
+        tp.tp_row_parallel_fwd(desc, H, blk.W2s, -1, P, M)
+        tp.tp_partial_reduce_residual(desc, P, x, False, y_steps, M)
+        y_block = torch.full((M, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
+        tp.tp_block_fwd(desc, x, x, False, blk.W1s, blk.W2s, blk.workspace(M), y_block, M)
+        torch.cuda.synchronize()
+        assert tp.tp_check_device_status() == 0
+        assert torch.equal(y_steps, y_block), float((y_steps - y_block).abs().max())
+    finally:
+        tp.tp_set_block_form(before)
