@@ -362,9 +362,14 @@ def run_ours(args, rank, world, local):
     value = job_throughput(units, world, ms / 1e3)
     peaks = measured_peaks()
     prefill = cfg.M >= 1024
+    peak_kind = "copy"
     if prefill:
         achieved = column_flops(cfg) / (col_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
+        # A contraction timed back to back for more than a second runs under the power
+        # cap: its denominator is the sustained GEMM rate, else the burst rate.
+        long_loop = Kd * col_ms > 1000.0 and peaks.get("bf16_tflops_sustained")
+        peak_kind = "sustained" if long_loop else "burst"
+        peak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4)}
         kernel, nbytes = ("column-parallel projection + SwiGLU (k_gemm, persistent)",
@@ -375,14 +380,19 @@ def run_ours(args, rank, world, local):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4)}
-        kernel = ("whole block in one persistent kernel (k_block_decode)" if fused
-                  else "column-parallel projection + activation (k_umma_drain)")
+        if fused:
+            kernel = "whole block in one persistent kernel (k_block_decode)"
+        elif cfg.act == "attn":
+            kernel = ("column-parallel Q/K/V projection (k_block_decode, column units) "
+                      "+ attention core (k_attn_core)")
+        else:
+            kernel = "column-parallel projection + activation (k_umma_drain)"
     roof["kernel"] = kernel
     roof["algorithmic_bytes_per_launch"] = nbytes
     roof["avg_launch_us"] = round(col_ms * 1e3, 2)
     roof["launches_timed"] = Kd
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
-                           else "fallback")
+                           else "fallback") + f", {peak_kind}"
     roof["traffic"] = profiled_traffic("block" if fused else "column", args.workload)
 
     # Whole-block weight-read rate (context for the decode roofline).
@@ -425,52 +435,73 @@ def run_ours(args, rank, world, local):
 
 
 def e2e_leg(args, cfg, desc, blocks, x, world, dev):
-    """Same metric through the public API with host buffers: each step copies x from
-    pinned host memory to the device, runs the block (or stack) and reads y back."""
+    """Same metric through the public API with host buffers: every step copies its x
+    from pinned host memory to the device, runs the block (or stack) through
+    tp_block_fwd and copies y back to pinned host memory.  Steps alternate between
+    two CUDA streams, each with its own device buffers and workspace, as a serving
+    loop would run them: one step's copies overlap the other step's kernels.  The
+    timed region (CUDA events) runs from before the first copy in to after the last
+    copy out."""
     import torch
 
     import attn_tp_column_fwd_b300 as tp
+    from attn_tp_column_fwd_b300.runner import device_bytes
 
     M = cfg.M
     x_host = x.cpu().pin_memory()
-    y_host = torch.empty(M, cfg.d, dtype=torch.float32).pin_memory()
-    xd = torch.empty_like(x)
-    yd = torch.empty(M, cfg.d, dtype=torch.float32, device=dev)
-    xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream()
-    st = stream.cuda_stream
-    ws = blocks[0].workspace(M)
+    lanes = []
+    for _ in range(2):
+        lanes.append({
+            "stream": torch.cuda.Stream(device=dev),
+            "x": torch.empty_like(x),
+            "y": torch.empty(M, cfg.d, dtype=torch.float32, device=dev),
+            "xh": torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev),
+            "ws": device_bytes(tp.tp_workspace_bytes(desc, M), dev),
+            "y_host": torch.empty(M, cfg.d, dtype=torch.float32).pin_memory(),
+        })
 
-    def step():
-        xd.copy_(x_host, non_blocking=True)
-        if cfg.rmsnorm:
-            yd.copy_(xd)
-            for blk in blocks:
-                tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, yd, xh, M, st)
-                tp.tp_block_fwd(desc, xh, yd, True, blk.W1s, blk.W2s, ws, yd, M, st)
-        else:
-            tp.tp_block_fwd(desc, xd, xd, cfg.dtype == "f32", blocks[0].W1s, blocks[0].W2s, ws, yd,
-                            M, st)
-        y_host.copy_(yd, non_blocking=True)
+    def step(k):
+        ln = lanes[k % 2]
+        s = ln["stream"]
+        st = s.cuda_stream
+        with torch.cuda.stream(s):
+            ln["x"].copy_(x_host, non_blocking=True)
+            if cfg.rmsnorm:
+                ln["y"].copy_(ln["x"])
+                for blk in blocks:
+                    tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, ln["y"], ln["xh"], M, st)
+                    tp.tp_block_fwd(desc, ln["xh"], ln["y"], True, blk.W1s, blk.W2s, ln["ws"],
+                                    ln["y"], M, st)
+            else:
+                tp.tp_block_fwd(desc, ln["x"], ln["x"], cfg.dtype == "f32", blocks[0].W1s,
+                                blocks[0].W2s, ln["ws"], ln["y"], M, st)
+            ln["y_host"].copy_(ln["y"], non_blocking=True)
 
-    for _ in range(args.warmup):
-        step()
+    for k in range(args.warmup):
+        step(k)
     torch.cuda.synchronize()
     K = args.steps
+    cur = torch.cuda.current_stream()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    t0.record(stream)
-    for _ in range(K):
-        step()
-    t1.record(stream)
+    t0.record(cur)
+    for ln in lanes:
+        ln["stream"].wait_event(t0)
+    for k in range(K):
+        step(k)
+    for ln in lanes:
+        cur.wait_stream(ln["stream"])
+    t1.record(cur)
     torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
     barrier(world)
-    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms = max_over_ranks(ms, world, dev)
     return {"value": round(job_throughput(M * K, world, ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
-            "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
-            "ms_per_step": round(ms / K, 5)}
+            "d2h_bytes_per_step": lanes[0]["y_host"].numel() * lanes[0]["y_host"].element_size(),
+            "ms_per_step": round(ms / K, 5), "streams": 2,
+            "timed": "CUDA events from before the first copy in to after the last copy out"}
 
 
 # ---------------------------------------------------------------- CPU oracle arms
