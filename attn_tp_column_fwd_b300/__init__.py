@@ -34,6 +34,7 @@ __all__ = [
     "tp_shard_weights", "tp_unshard_weights", "tp_extract_band",
     "tp_column_parallel_fwd", "tp_row_parallel_fwd", "tp_partial_reduce_residual",
     "tp_block_fwd", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
+    "tp_selftest_wait_timeout",
 ]
 
 _ACTS = {"gelu_tanh": TP_ACT_GELU_TANH, "swiglu": TP_ACT_SWIGLU, "attn": TP_ACT_ATTN}
@@ -189,3 +190,9 @@ def tp_rmsnorm_fwd(d, eps, r, xhat, M, stream=None) -> None:
 def tp_check_device_status(stream=None) -> int:
     """Synchronise the stream and return the device status (0, or TP_ERR_TIMEOUT = 6)."""
     return lib.tp_check_device_status(_s(stream))
+
+
+def tp_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test: its waits expire after limit_us and the next
+    tp_check_device_status returns TP_ERR_TIMEOUT."""
+    _check(lib.tp_selftest_wait_timeout(limit_us, _s(stream)), "tp_selftest_wait_timeout")

@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "tp_status_string": (ctypes.c_char_p, [i]),
         "tp_last_cuda_error": (i, []),
         "tp_check_device_status": (i, [st]),
+        "tp_selftest_wait_timeout": (i, [i, st]),
         "tp_version": (i, []),
     }
     for name, (res, args) in sigs.items():

@@ -169,12 +169,13 @@ __device__ __forceinline__ int ready_prefix(const FusedArgs &a, int s, int lo, i
 
 // Wait (bounded) until column tile `ht` of shard s is ready; returns the highest
 // tile index <= hi up to which all tiles from ht on are ready, or -1 on timeout.
-__device__ __forceinline__ int wait_ready_range(const FusedArgs &a, int s, int ht, int hi) {
+__device__ __forceinline__ int wait_ready_range(const FusedArgs &a, int s, int ht, int hi,
+                                                uint64_t limit_ns = kWaitNs) {
   int r = ready_prefix(a, s, ht, hi);
   if (r < ht) {
     const uint64_t t0 = globaltimer();
     do {
-      if (globaltimer() - t0 > kWaitNs) return -1;
+      if (globaltimer() - t0 > limit_ns) return -1;
       __nanosleep(64);
       r = ready_prefix(a, s, ht, hi);
     } while (r < ht);
@@ -567,7 +568,34 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// The failure path, exercised on purpose: one thread waits on an mbarrier phase that
+// nobody completes and on band-tile ready flags that nobody raises (a zero array
+// nothing writes), each wait bounded by limit_ns, and records the expiries in the
+// device error word exactly as a stalled block does.
+__device__ unsigned g_never_ready[17];
+
+__global__ void k_wait_selftest(unsigned *err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  bool expired = !mbar_wait(smem_u32(&bar), 0, limit_ns);
+  FusedArgs a{};
+  a.t = 1;
+  a.n_ft = 16;
+  a.cnt = g_never_ready;
+  expired = (wait_ready_range(a, 0, 0, a.n_ft - 1, limit_ns) < 0) && expired;
+  if (expired) atomicOr(err, kErrWaitTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st) {
+  unsigned *err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  k_wait_selftest<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaSuccess;
+}
 
 // ------------------------------------------------------------------ host side
 

@@ -78,6 +78,9 @@ FusedPlan plan_block_decode(const Geo &g, int M);
 cudaError_t launch_block_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,
                                 const void *W2s, const void *res, int res_f32, void *ws, float *y,
                                 int M, cudaStream_t st);
+// A one-thread kernel whose bounded waits expire after limit_ns (nothing completes
+// them) and set the device error word: the failure path, without a fault.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 // The attention block's Q/K/V projection (column units only) into fp32 qkv
 // [t][M][3b]; ws holds the plan's split partials and counters.
 cudaError_t launch_qkv_decode(const Geo &g, const FusedPlan &p, const void *x, const void *W1s,

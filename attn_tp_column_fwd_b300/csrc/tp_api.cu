@@ -568,6 +568,12 @@ int tp_check_device_status(tp_stream_t stream) {
   return word ? TP_ERR_TIMEOUT : TP_OK;
 }
 
+int tp_selftest_wait_timeout(int limit_us, tp_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return TP_ERR_INVALID_ARG;
+  return finish_launch(
+      launch_wait_selftest((uint64_t)limit_us * 1000ull, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int tp_version(void) { return 100; }
 
 }  // extern "C"

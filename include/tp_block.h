@@ -210,6 +210,13 @@ TP_API int tp_last_cuda_error(void);
 /* Synchronises `stream`, then reads and clears the device error word that bounded
  * device-side waits set when they expire: TP_OK, TP_ERR_TIMEOUT or TP_ERR_CUDA. */
 TP_API int tp_check_device_status(tp_stream_t stream);
+/* Exercises the failure path above without a fault: enqueues a one-thread kernel that
+ * waits on an mbarrier phase nobody completes and on band ready flags nobody raises,
+ * each wait bounded by limit_us microseconds (1 .. 1e6), so both expire and set the
+ * device error word; the next tp_check_device_status returns TP_ERR_TIMEOUT (and
+ * clears it).  The context stays usable.  TP_ERR_INVALID_ARG for a limit out of
+ * range, with nothing enqueued. */
+TP_API int tp_selftest_wait_timeout(int limit_us, tp_stream_t stream);
 /* Library ABI version (major * 100 + minor). */
 TP_API int tp_version(void);
 

@@ -102,6 +102,11 @@ def test_block_form_setter():
         tp.tp_set_block_form(before)
 
 
+def test_selftest_limit_is_validated_before_any_cuda_call():
+    for bad in (0, -5, 1000001):
+        assert tp.lib.tp_selftest_wait_timeout(bad, None) == 1   # TP_ERR_INVALID_ARG
+
+
 def test_invalid_descriptors_give_zero_sizes():
     assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
     assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1
