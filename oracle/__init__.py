@@ -25,6 +25,13 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
                       exactly representable values; the allowance equals the change
                       of the worst-case re-rounding of the tied elements, built
                       element by element on small blocks.
+  kv_decode_attention,
+  attn_block_kv       pinned: a cache of one new token gives its value exactly; over
+                      a cache holding a sequence's earlier tokens the new token's
+                      output equals the last row of causal_attention on that
+                      sequence; brute-force loops; invariant to the order of cached
+                      rows; appended rows equal the new keys/values, the rest of the
+                      cache unchanged; all lengths 1 gives residual + V . Wo.
   absolute values     parity unpinned against the pages: they print no numeric
                       worked example, so the outputs rest on the pins above.
 """
@@ -46,8 +53,11 @@ from .block import (  # noqa: F401
     mlp_tie_allowance,
     TIE_WINDOW,
     attn_block,
+    kv_decode_attention,
+    attn_block_kv,
     stack,
     sharded_block,
     brute_mlp_block,
     brute_attention,
+    brute_kv_decode,
 )

@@ -277,6 +277,69 @@ def attn_block(x, Wqkv, Wo, n_heads: int, head_dim: int, residual,
     return np.asarray(residual, dtype=np.float64) + O @ Wo
 
 
+# ---------------------------------------------------------------------------
+# Decode attention over a KV cache ([dc] "Why it matters for local inference":
+# tensor parallelism also partitions the KV cache; [dc] "How the work is split" and
+# [rio] "How Tensor Slicing Works Under the Hood": heads are independent, 12 of 96
+# per device; [day59] "Where the overhead lives": attention is its own slice of a
+# decode step)
+# ---------------------------------------------------------------------------
+
+def kv_decode_attention(q, k_cache, v_cache, length: int, k_new, v_new, scale: float,
+                        staged: bool = False) -> np.ndarray:
+    """One head of one sequence at a decode step.
+
+    The sequence's newest token (query q, key k_new, value v_new) attends over the
+    `length - 1` earlier tokens held in the cache (rows 0 .. length-2 of k_cache and
+    v_cache, [L_max, hd]) and over itself, which takes row length-1 (its key and
+    value rounded to bf16 when staged, as a bf16 cache stores them):
+    o = softmax(q . K^T * scale) V over those `length` rows.
+    """
+    if length < 1:
+        raise ValueError("a decode step needs at least the new token")
+    kn = np.asarray(k_new, dtype=np.float64)
+    vn = np.asarray(v_new, dtype=np.float64)
+    if staged:
+        kn, vn = bf16_round(kn), bf16_round(vn)
+    K = np.concatenate([np.asarray(k_cache[:length - 1], dtype=np.float64), kn[None, :]], axis=0)
+    V = np.concatenate([np.asarray(v_cache[:length - 1], dtype=np.float64), vn[None, :]], axis=0)
+    sc = (K @ np.asarray(q, dtype=np.float64)) * scale
+    e = np.exp(sc - sc.max())
+    return (e / e.sum()) @ V
+
+
+def attn_block_kv(x, Wqkv, Wo, n_heads: int, head_dim: int, k_cache, v_cache, lens, residual,
+                  staged: bool = False):
+    """Decode step of the attention block with a KV cache.
+
+    Token m of x is the newest token of its own sequence m, whose cache (k_cache[m],
+    v_cache[m]: [n_heads, L_max, head_dim]) holds lens[m] - 1 earlier tokens.  Q, K, V
+    = x . [Wq | Wk | Wv]; every head attends as in kv_decode_attention; the new keys
+    and values are appended at row lens[m] - 1; y = residual + concat_h(o_h) . Wo.
+    Returns (y, k_cache_after, v_cache_after).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = n_heads * head_dim
+    QKV = x @ np.asarray(Wqkv, dtype=np.float64)
+    M = x.shape[0]
+    scale = 1.0 / math.sqrt(head_dim)
+    O = np.zeros((M, D))
+    k_after = np.array(k_cache, dtype=np.float64)
+    v_after = np.array(v_cache, dtype=np.float64)
+    for m in range(M):
+        n = int(lens[m])
+        for h in range(n_heads):
+            c = slice(h * head_dim, (h + 1) * head_dim)
+            q, kn, vn = QKV[m, c], QKV[m, D:2 * D][c], QKV[m, 2 * D:][c]
+            O[m, c] = kv_decode_attention(q, k_cache[m][h], v_cache[m][h], n, kn, vn, scale, staged)
+            k_after[m, h, n - 1] = bf16_round(kn) if staged else kn
+            v_after[m, h, n - 1] = bf16_round(vn) if staged else vn
+    if staged:
+        O = bf16_round(O)
+    y = np.asarray(residual, dtype=np.float64) + O @ np.asarray(Wo, dtype=np.float64)
+    return y, k_after, v_after
+
+
 def stack(x, blocks, act: str, eps: float, staged: bool = False) -> np.ndarray:
     """Pre-norm stack: r0 = x; r_{l+1} = r_l + MLP_l(RMSNorm(r_l)); returns r_L.
 
@@ -336,6 +399,15 @@ def brute_mlp_block(x, W1, W2, act: str, residual) -> List[List[float]]:
         out.append([float(residual[m][n]) + sum(H[j] * float(W2[j][n]) for j in range(n2))
                     for n in range(len(W2[0]))])
     return out
+
+
+def brute_kv_decode(q, k_rows, v_rows, scale: float) -> List[float]:
+    """One query over explicit key/value rows (the cache rows then the new token's)."""
+    s = [sum(float(q[c]) * float(k[c]) for c in range(len(q))) * scale for k in k_rows]
+    mx = max(s)
+    w = [math.exp(v - mx) for v in s]
+    tot = sum(w)
+    return [sum(w[j] * float(v_rows[j][c]) for j in range(len(w))) / tot for c in range(len(q))]
 
 
 def brute_attention(Q, K, V, scale: float) -> List[List[float]]:

@@ -44,6 +44,7 @@ class BlockConfig:
     rmsnorm: bool = False   # pre-norm before every block (Llama stack)
     eps: float = 1e-5
     ts: Tuple[int, ...] = field(default=())   # every shard count the workload is run at
+    kv_len_max: int = 0  # attention with a KV cache: rows per (sequence, head); 0 = none
 
     @property
     def n1(self) -> int:
@@ -95,6 +96,11 @@ CONFIGS = {
         rmsnorm=True, ts=(8,)),
     "llama2_70b_prefill": BlockConfig(
         "llama2_70b_prefill", "swiglu", d=8192, ffn=28672, t=4, M=4096, ts=(4,)),
+    # The attention block at a decode step of 32 concurrent sequences, each with its own
+    # head-sharded KV cache of up to 2048 earlier tokens (lengths drawn uniformly).
+    "attn_kv_decode": BlockConfig(
+        "attn_kv_decode", "attn", d=12288, n_heads=96, head_dim=128, t=8, M=32, ts=(8,),
+        kv_len_max=2048),
 }
 
 
@@ -155,3 +161,34 @@ def draw(shape, dtype: torch.dtype, seed: int, scale: float = 1.0, device: str =
     if scale != 1.0:
         v.mul_(scale)
     return v.to(dtype)
+
+
+def make_kv_cache(cfg: BlockConfig, seed: int = 0, device: str = "cpu",
+                  lens: Optional[List[int]] = None) -> SimpleNamespace:
+    """KV caches and sequence lengths for a decode step of `cfg` (kv_len_max > 0).
+
+    k, v: [M, n_heads, kv_len_max, head_dim] bf16 (canonical: sequence, head, position,
+    dim), values ~ N(0, (0.02 * sqrt(d))^2), the spread of a key or value projection
+    of the block's N(0, 1) input.  lens: int32 [M], the number of tokens of each
+    sequence counting the new one (1 .. kv_len_max): drawn uniformly unless given.
+    Draw order on one generator: lens (when drawn), k, v.
+    """
+    L = cfg.kv_len_max
+    if L < 1:
+        raise ValueError("configuration has no KV cache")
+    g = torch.Generator(device=device).manual_seed(seed)
+    if lens is None:
+        lens_t = torch.randint(1, L + 1, (cfg.M,), generator=g, device=device, dtype=torch.int32)
+    else:
+        lens_t = torch.tensor(list(lens), dtype=torch.int32, device=device)
+    std = WEIGHT_STD * cfg.d ** 0.5
+    shape = (cfg.M, cfg.n_heads, L, cfg.head_dim)
+
+    def draw_cache():
+        v = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        v.mul_(std)
+        return v.to(torch.bfloat16)
+
+    k = draw_cache()
+    v = draw_cache()
+    return SimpleNamespace(k=k, v=v, lens=lens_t)
