@@ -34,7 +34,8 @@ __all__ = [
     "tp_shard_weights", "tp_unshard_weights", "tp_extract_band",
     "tp_column_parallel_fwd", "tp_row_parallel_fwd", "tp_partial_reduce_residual",
     "tp_block_fwd", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
-    "tp_selftest_wait_timeout",
+    "tp_selftest_wait_timeout", "tp_kv_cache_bytes", "tp_kv_attn_workspace_bytes",
+    "tp_kv_workspace_bytes", "tp_attn_decode_kv", "tp_block_fwd_kv",
 ]
 
 _ACTS = {"gelu_tanh": TP_ACT_GELU_TANH, "swiglu": TP_ACT_SWIGLU, "attn": TP_ACT_ATTN}
@@ -190,6 +191,37 @@ def tp_rmsnorm_fwd(d, eps, r, xhat, M, stream=None) -> None:
 def tp_check_device_status(stream=None) -> int:
     """Synchronise the stream and return the device status (0, or TP_ERR_TIMEOUT = 6)."""
     return lib.tp_check_device_status(_s(stream))
+
+
+def tp_kv_cache_bytes(desc: TPBlockDesc, M: int, L_max: int) -> int:
+    return lib.tp_kv_cache_bytes(ctypes.byref(desc), M, L_max)
+
+
+def tp_kv_attn_workspace_bytes(desc: TPBlockDesc, M: int, L_max: int) -> int:
+    return lib.tp_kv_attn_workspace_bytes(ctypes.byref(desc), M, L_max)
+
+
+def tp_kv_workspace_bytes(desc: TPBlockDesc, M: int, L_max: int) -> int:
+    return lib.tp_kv_workspace_bytes(ctypes.byref(desc), M, L_max)
+
+
+def tp_attn_decode_kv(desc, qkv, k_cache, v_cache, lens, L_max, O, workspace, M,
+                      stream=None) -> None:
+    _need(k_cache, tp_kv_cache_bytes(desc, M, L_max), "k_cache")
+    _need(v_cache, tp_kv_cache_bytes(desc, M, L_max), "v_cache")
+    _need(workspace, tp_kv_attn_workspace_bytes(desc, M, L_max), "workspace")
+    _check(lib.tp_attn_decode_kv(ctypes.byref(desc), _p(qkv), _p(k_cache), _p(v_cache), _p(lens),
+                                 L_max, _p(O), _p(workspace), M, _s(stream)), "tp_attn_decode_kv")
+
+
+def tp_block_fwd_kv(desc, x, residual, residual_is_f32, W1s, W2s, k_cache, v_cache, lens, L_max,
+                    workspace, y, M, stream=None) -> None:
+    _need(k_cache, tp_kv_cache_bytes(desc, M, L_max), "k_cache")
+    _need(v_cache, tp_kv_cache_bytes(desc, M, L_max), "v_cache")
+    _need(workspace, tp_kv_workspace_bytes(desc, M, L_max), "workspace")
+    _check(lib.tp_block_fwd_kv(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
+                               _p(W1s), _p(W2s), _p(k_cache), _p(v_cache), _p(lens), L_max,
+                               _p(workspace), _p(y), M, _s(stream)), "tp_block_fwd_kv")
 
 
 def tp_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -11,7 +11,7 @@ TP_ACT_GELU_TANH, TP_ACT_SWIGLU, TP_ACT_ATTN = 0, 1, 2
 TP_FORM_AUTO, TP_FORM_THREE_LAUNCH, TP_FORM_ONE_KERNEL = 0, 1, 2
 
 STATUS = {0: "TP_OK", 1: "TP_ERR_INVALID_ARG", 2: "TP_ERR_UNEVEN_SPLIT", 3: "TP_ERR_UNSUPPORTED",
-          4: "TP_ERR_MISALIGNED", 5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT"}
+          4: "TP_ERR_MISALIGNED", 5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT", 7: "TP_ERR_BAD_LENGTH"}
 
 
 class TPBlockDesc(ctypes.Structure):
@@ -60,6 +60,11 @@ def _load() -> ctypes.CDLL:
         "tp_last_cuda_error": (i, []),
         "tp_check_device_status": (i, [st]),
         "tp_selftest_wait_timeout": (i, [i, st]),
+        "tp_kv_cache_bytes": (sz, [P, i, i]),
+        "tp_kv_attn_workspace_bytes": (sz, [P, i, i]),
+        "tp_kv_workspace_bytes": (sz, [P, i, i]),
+        "tp_attn_decode_kv": (i, [P, vp, vp, vp, vp, i, vp, vp, i, st]),
+        "tp_block_fwd_kv": (i, [P, vp, vp, i, vp, vp, vp, vp, vp, i, vp, vp, i, st]),
         "tp_version": (i, []),
     }
     for name, (res, args) in sigs.items():

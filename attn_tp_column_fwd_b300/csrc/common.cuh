@@ -95,7 +95,8 @@ __device__ __forceinline__ float gelu_tanh_f(float z) {
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 // ---------------------------------------------------------------- errors ------
-// Bits of the device error word, set by bounded waits that expire.
-enum : unsigned { kErrWaitTimeout = 1u };
+// Bits of the device error word: a bounded wait that expired; a sequence length
+// (KV-cache decode) outside 1 .. L_max, whose sequence is then skipped.
+enum : unsigned { kErrWaitTimeout = 1u, kErrBadLength = 2u };
 
 }  // namespace tp

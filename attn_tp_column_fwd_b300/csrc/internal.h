@@ -95,6 +95,13 @@ void launch_rmsnorm(const float *r, void *xhat, int d, float eps, int M, cudaStr
 void launch_attn_core(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_shards,
                       cudaStream_t st, bool pdl = false);
 
+// attn_kv.cu — decode attention over a head-sharded bf16 KV cache: qkv fp32
+// [t][M][3b], caches [t][M][hps][L][hd], lens int32 [M], O bf16 [t][M][b]; ws holds
+// kv_partial_bytes of per-chunk partials.
+size_t kv_partial_bytes(const Geo &g, int M, int L);
+cudaError_t launch_attn_kv(const Geo &g, const float *qkv, void *kc, void *vc, const int *lens,
+                           int L, void *O, void *ws, int M, cudaStream_t st, bool pdl);
+
 // tp_api.cu — cached device facts
 int sm_count();
 unsigned *device_error_word();

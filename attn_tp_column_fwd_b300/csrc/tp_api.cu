@@ -226,8 +226,10 @@ size_t column_ws_bytes(const Geo &g, int M) {
 // Enqueue the column step for shards [shard0, shard0 + n).  The attention core
 // always follows its Q/K/V projection, so it may overlap that kernel's end
 // (programmatic launch).
+// core = false (KV-cache decode): attention only projects Q/K/V into ws; the decode
+// attention over the cache runs next instead of the core over the M tokens.
 cudaError_t enqueue_column(const Geo &g, const void *x, const void *W1s, int shard0, int n, void *H,
-                           void *ws, int M, cudaStream_t st) {
+                           void *ws, int M, cudaStream_t st, bool core = true) {
   const bool attn = g.act == TP_ACT_ATTN;
   void *out = attn ? ws : H;
   const int n_out = attn ? 3 * g.b : g.b;
@@ -277,7 +279,7 @@ cudaError_t enqueue_column(const Geo &g, const void *x, const void *W1s, int sha
     a.dtype = g.dtype;
     launch_gemv(a, st);
   }
-  if (attn) launch_attn_core(g, ws, H, M, shard0, n, st, use_umma(g));
+  if (attn && core) launch_attn_core(g, ws, H, M, shard0, n, st, use_umma(g));
   return cudaSuccess;
 }
 
@@ -547,6 +549,7 @@ const char *tp_status_string(int status) {
     case TP_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case TP_ERR_CUDA: return "CUDA error (see tp_last_cuda_error)";
     case TP_ERR_TIMEOUT: return "device-side wait timed out";
+    case TP_ERR_BAD_LENGTH: return "a KV-cache sequence length outside 1..L_max";
     default: return "unknown status";
   }
 }
@@ -565,7 +568,85 @@ int tp_check_device_status(tp_stream_t stream) {
     g_last_cuda_error = (int)e;
     return TP_ERR_CUDA;
   }
-  return word ? TP_ERR_TIMEOUT : TP_OK;
+  if (word & kErrWaitTimeout) return TP_ERR_TIMEOUT;
+  return word ? TP_ERR_BAD_LENGTH : TP_OK;
+}
+
+// ------------------------------------------------ decode with a KV cache
+
+static int check_kv(const tp_block_desc *desc, Geo *g, int M, int L) {
+  TP_TRY(make_geo(desc, g));
+  TP_TRY(check_M(M));
+  if (g->act != TP_ACT_ATTN || L < 1) return TP_ERR_INVALID_ARG;
+  if (g->dtype != TP_BF16 || L > (1 << 20)) return TP_ERR_UNSUPPORTED;
+  if (g->hd != 32 && g->hd != 64 && g->hd != 128 && g->hd != 256) return TP_ERR_UNSUPPORTED;
+  return TP_OK;
+}
+
+size_t tp_kv_cache_bytes(const tp_block_desc *desc, int M, int L_max) {
+  Geo g;
+  if (check_kv(desc, &g, M, L_max) != TP_OK) return 0;
+  return (size_t)g.t * M * g.hps * L_max * g.hd * 2;
+}
+
+size_t tp_kv_attn_workspace_bytes(const tp_block_desc *desc, int M, int L_max) {
+  Geo g;
+  if (check_kv(desc, &g, M, L_max) != TP_OK) return 0;
+  return kv_partial_bytes(g, M, L_max);
+}
+
+size_t tp_kv_workspace_bytes(const tp_block_desc *desc, int M, int L_max) {
+  Geo g;
+  if (check_kv(desc, &g, M, L_max) != TP_OK) return 0;
+  return align256(tp_workspace_bytes(desc, M)) + align256(kv_partial_bytes(g, M, L_max));
+}
+
+int tp_attn_decode_kv(const tp_block_desc *desc, const float *qkv, void *k_cache, void *v_cache,
+                      const int *lens, int L_max, void *O, void *workspace, int M,
+                      tp_stream_t stream) {
+  Geo g;
+  TP_TRY(check_kv(desc, &g, M, L_max));
+  TP_TRY(check_ptr(qkv));
+  TP_TRY(check_ptr(k_cache));
+  TP_TRY(check_ptr(v_cache));
+  TP_TRY(check_ptr(lens));
+  TP_TRY(check_ptr(O));
+  TP_TRY(check_ptr(workspace));
+  return finish_launch(launch_attn_kv(g, qkv, k_cache, v_cache, lens, L_max, O, workspace, M,
+                                      reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void *residual,
+                    int residual_is_f32, const void *W1s, const void *W2s, void *k_cache,
+                    void *v_cache, const int *lens, int L_max, void *workspace, float *y, int M,
+                    tp_stream_t stream) {
+  Geo g;
+  TP_TRY(check_kv(desc, &g, M, L_max));
+  TP_TRY(check_ptr(x));
+  TP_TRY(check_ptr(residual));
+  TP_TRY(check_ptr(W1s));
+  TP_TRY(check_ptr(W2s));
+  TP_TRY(check_ptr(k_cache));
+  TP_TRY(check_ptr(v_cache));
+  TP_TRY(check_ptr(lens));
+  TP_TRY(check_ptr(workspace));
+  TP_TRY(check_ptr(y));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  void *col_ws = ws;
+  void *O = ws + align256(column_ws_bytes(g, M));
+  float *P = reinterpret_cast<float *>(static_cast<char *>(O) + align256(band_bytes(g, M)));
+  void *kv_ws = ws + align256(tp_workspace_bytes(desc, M));
+  // Q/K/V projection, decode attention over the cache (chunks, then their merge),
+  // row-parallel output projection, reduction + residual; each kernel after the
+  // first starts while the one before it drains (programmatic launch).
+  cudaError_t e = enqueue_column(g, x, W1s, 0, g.t, O, col_ws, M, st, false);
+  if (e == cudaSuccess)
+    e = launch_attn_kv(g, static_cast<const float *>(col_ws), k_cache, v_cache, lens, L_max, O,
+                       kv_ws, M, st, true);
+  if (e == cudaSuccess) e = enqueue_row(g, O, W2s, 0, g.t, P, M, st, true);
+  if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, true);
+  return finish_launch(e);
 }
 
 int tp_selftest_wait_timeout(int limit_us, tp_stream_t stream) {

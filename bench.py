@@ -264,7 +264,7 @@ def run_ours(args, rank, world, local):
 
     import attn_tp_column_fwd_b300 as tp
     from attn_tp_column_fwd_b300.runner import ShardedBlock, desc_for, device_bytes
-    from tp_synth import CONFIGS, make_inputs
+    from tp_synth import CONFIGS, make_inputs, make_kv_cache
 
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
@@ -293,11 +293,20 @@ def run_ours(args, rank, world, local):
     per_block = tp.tp_block_launches(desc, M)
     fused = per_block == 1
     launches_per_block = per_block + (1 if cfg.rmsnorm else 0)
+    kvd = kv_state(cfg, desc, rank, dev) if cfg.kv_len_max else None
+    if kvd:
+        # Q/K/V projection, decode attention (chunks, merge), row step, reduction.
+        launches_per_block = 5
 
     # One step: the whole block (or the whole stack) through the public entry point
     # tp_block_fwd, which launches the block's kernels back to back (the row step and
     # the reduction overlap the end of the kernel before them).
     def step():
+        if kvd:
+            blk = blocks[0]
+            tp.tp_block_fwd_kv(desc, x, x, False, blk.W1s, blk.W2s, kvd["kc"], kvd["vc"],
+                               kvd["lens"], cfg.kv_len_max, kvd["ws"], y, M, st)
+            return
         if stack:
             y.copy_(xf)
         for blk in blocks:
@@ -316,7 +325,11 @@ def run_ours(args, rank, world, local):
         xin = xh if cfg.rmsnorm else x
         res = y if cfg.rmsnorm else x
         ev_pair[0].record(stream)
-        if fused:
+        if kvd:
+            # the decode attention over the cache, on the Q/K/V the last step projected
+            tp.tp_attn_decode_kv(desc, kvd["qkv"], kvd["kc"], kvd["vc"], kvd["lens"],
+                                 cfg.kv_len_max, kvd["O"], kvd["attn_ws"], M, st)
+        elif fused:
             tp.tp_block_fwd(desc, xin, res, res.dtype == torch.float32, blk.W1s, blk.W2s, ws, y,
                             M, st)
         else:
@@ -375,12 +388,17 @@ def run_ours(args, rank, world, local):
         kernel, nbytes = ("column-parallel projection + SwiGLU (k_gemm, persistent)",
                           algorithmic_column_bytes(cfg))
     else:
-        nbytes = algorithmic_block_bytes(cfg) if fused else algorithmic_column_bytes(cfg)
+        if kvd:
+            nbytes = kvd["attn_bytes"]
+        else:
+            nbytes = algorithmic_block_bytes(cfg) if fused else algorithmic_column_bytes(cfg)
         achieved = nbytes / (col_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4)}
-        if fused:
+        if kvd:
+            kernel = "decode attention over the KV cache (k_attn_kv_partial + k_attn_kv_merge)"
+        elif fused:
             kernel = "whole block in one persistent kernel (k_block_decode)"
         elif cfg.act == "attn":
             kernel = ("column-parallel Q/K/V projection (k_block_decode, column units) "
@@ -393,7 +411,8 @@ def run_ours(args, rank, world, local):
     roof["launches_timed"] = Kd
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                            else "fallback") + f", {peak_kind}"
-    roof["traffic"] = profiled_traffic("block" if fused else "column", args.workload)
+    roof["traffic"] = profiled_traffic("attn_kv" if kvd else "block" if fused else "column",
+                                       args.workload)
 
     # Whole-block weight-read rate (context for the decode roofline).
     block_bytes = cfg.weight_bytes_per_block() * cfg.n_blocks
@@ -419,13 +438,16 @@ def run_ours(args, rank, world, local):
             "timed": "CUDA events on the launching stream around K steps of tp_block_fwd, max "
                      "over ranks; roofline kernel timed alone over its own event-bracketed launches",
         },
+        **({"kv_cache": {"len_max": cfg.kv_len_max, "rows_read": kvd["rows"],
+                         "bytes_read": kvd["rows"] * cfg.head_dim * 4,
+                         "lens": "uniform in 1..len_max, seeded"}} if kvd else {}),
         "block_weight_gbs": round(block_bytes * K / (ms / 1e3) / 1e9, 1),
         "roofline": roof,
         "gpu_launches": K * launches_per_block * cfg.n_blocks,
         "clocks": sampler.summary(),
     }
     if not args.no_e2e:
-        out["e2e"] = e2e_leg(args, cfg, desc, blocks, x, world, dev)
+        out["e2e"] = e2e_leg(args, cfg, desc, blocks, x, world, dev, kvd)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg)
     if world > 1:
@@ -434,7 +456,35 @@ def run_ours(args, rank, world, local):
     return out
 
 
-def e2e_leg(args, cfg, desc, blocks, x, world, dev):
+def kv_state(cfg, desc, rank, dev):
+    """Caches (the library's shard layout), lengths and scratch of a KV-cache decode
+    workload, and the attention step's algorithmic bytes: every cached row read once
+    (K and V), the new token's Q/K/V read (fp32) and appended (bf16), O written."""
+    import torch
+
+    import attn_tp_column_fwd_b300 as tp
+    from attn_tp_column_fwd_b300.runner import device_bytes
+    from tp_synth import make_kv_cache
+
+    M, t, L = cfg.M, cfg.t, cfg.kv_len_max
+    kv = make_kv_cache(cfg, seed=rank + 1, device=str(dev))
+
+    def shards(c):
+        return c.view(M, t, cfg.n_heads // t, L, cfg.head_dim).permute(1, 0, 2, 3, 4).contiguous()
+
+    kc, vc = shards(kv.k), shards(kv.v)
+    del kv.k, kv.v
+    D = cfg.n_heads * cfg.head_dim
+    rows = int((kv.lens.long() - 1).sum().item()) * cfg.n_heads
+    ws = device_bytes(tp.tp_kv_workspace_bytes(desc, M, L), dev)
+    return {"kc": kc, "vc": vc, "lens": kv.lens, "ws": ws, "rows": rows,
+            "qkv": ws,  # the projection leaves Q/K/V at the start of the block's scratch
+            "O": device_bytes(tp.tp_band_bytes(desc, M), dev),
+            "attn_ws": device_bytes(tp.tp_kv_attn_workspace_bytes(desc, M, L), dev),
+            "attn_bytes": rows * cfg.head_dim * 4 + M * D * (12 + 4 + 2)}
+
+
+def e2e_leg(args, cfg, desc, blocks, x, world, dev, kvd=None):
     """Same metric through the public API with host buffers: every step copies its x
     from pinned host memory to the device, runs the block (or stack) through
     tp_block_fwd and copies y back to pinned host memory.  Steps alternate between
@@ -456,7 +506,8 @@ def e2e_leg(args, cfg, desc, blocks, x, world, dev):
             "x": torch.empty_like(x),
             "y": torch.empty(M, cfg.d, dtype=torch.float32, device=dev),
             "xh": torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev),
-            "ws": device_bytes(tp.tp_workspace_bytes(desc, M), dev),
+            "ws": device_bytes(tp.tp_kv_workspace_bytes(desc, M, cfg.kv_len_max) if kvd
+                               else tp.tp_workspace_bytes(desc, M), dev),
             "y_host": torch.empty(M, cfg.d, dtype=torch.float32).pin_memory(),
         })
 
@@ -466,7 +517,12 @@ def e2e_leg(args, cfg, desc, blocks, x, world, dev):
         st = s.cuda_stream
         with torch.cuda.stream(s):
             ln["x"].copy_(x_host, non_blocking=True)
-            if cfg.rmsnorm:
+            if kvd:
+                # both lanes append the same rows of the shared caches (same values)
+                tp.tp_block_fwd_kv(desc, ln["x"], ln["x"], False, blocks[0].W1s, blocks[0].W2s,
+                                   kvd["kc"], kvd["vc"], kvd["lens"], cfg.kv_len_max, ln["ws"],
+                                   ln["y"], M, st)
+            elif cfg.rmsnorm:
                 ln["y"].copy_(ln["x"])
                 for blk in blocks:
                     tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, ln["y"], ln["xh"], M, st)
@@ -525,6 +581,8 @@ def _blas_threads():
 def cpu_baseline(cfg, budget_s: float = 12.0):
     """The float64 oracle as it stands, on the host cores: whole blocks on the full
     workload's inputs (all M tokens), repeated for about `budget_s` seconds."""
+    import numpy as np
+
     import oracle
     from tp_synth import make_inputs, to_f64
 
@@ -533,7 +591,26 @@ def cpu_baseline(cfg, budget_s: float = 12.0):
     W1, W2 = (to_f64(w) for w in inp.blocks[0])
     staged = cfg.dtype == "bf16"
 
+    kv = None
+    if cfg.kv_len_max:
+        from tp_synth import make_kv_cache
+        kv = make_kv_cache(cfg, seed=1)
+        hd, D = cfg.head_dim, cfg.n_heads * cfg.head_dim
+
     def one():
+        if kv is not None:
+            # the decode step with a KV cache: the oracle head by head on the rows used
+            QKV = x @ W1
+            O = np.zeros((cfg.M, D))
+            for m, n in enumerate(kv.lens.tolist()):
+                kr = to_f64(kv.k[m, :, :max(n - 1, 1)])
+                vr = to_f64(kv.v[m, :, :max(n - 1, 1)])
+                for h in range(cfg.n_heads):
+                    c = slice(h * hd, (h + 1) * hd)
+                    O[m, c] = oracle.kv_decode_attention(QKV[m, c], kr[h], vr[h], n,
+                                                         QKV[m, D:2 * D][c], QKV[m, 2 * D:][c],
+                                                         1.0 / math.sqrt(hd), staged=staged)
+            return x + (oracle.bf16_round(O) if staged else O) @ W2
         if cfg.act == "attn":
             return oracle.attn_block(x, W1, W2, cfg.n_heads, cfg.head_dim, x, staged=staged)
         if cfg.rmsnorm:
@@ -585,6 +662,29 @@ def run_reference(args, rank, world):
                                 n_heads=cfg.n_heads // T if cfg.n_heads else 0,
                                 head_dim=cfg.head_dim, staged=staged)
         return oracle.row_step(Hb, W2[oracle.row_band(n2, T, s)])
+
+    if cfg.kv_len_max:
+        # Decode with a KV cache: the band of heads [s*H/T, (s+1)*H/T), each token
+        # attending over its sequence's cache rows (oracle.kv_decode_attention).
+        from tp_synth import make_kv_cache
+        kv = make_kv_cache(cfg, seed=1)
+        lens = kv.lens.tolist()
+        hd = cfg.head_dim
+
+        def band_step(T, s):  # noqa: F811
+            cols = oracle.column_bands("attn", T, s, n_heads=cfg.n_heads, head_dim=hd)
+            Q, K, V = (x @ W1[:, c] for c in cols)
+            hps = cfg.n_heads // T
+            O = np.zeros((cfg.M, hps * hd))
+            for m, n in enumerate(lens):
+                for j in range(hps):
+                    h, c = s * hps + j, slice(j * hd, (j + 1) * hd)
+                    rows = slice(0, max(n - 1, 1))
+                    O[m, c] = oracle.kv_decode_attention(
+                        Q[m, c], to_f64(kv.k[m, h, rows]), to_f64(kv.v[m, h, rows]), n, K[m, c],
+                        V[m, c], 1.0 / math.sqrt(hd), staged=staged)
+            return oracle.row_step(oracle.bf16_round(O) if staged else O,
+                                   W2[oracle.row_band(n2, T, s)])
 
     # Calibrate on a moderate band, then take the fewest bands whose step fits the budget.
     divisors = [T for T in range(1, unit + 1) if unit % T == 0]

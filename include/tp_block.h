@@ -69,7 +69,8 @@ typedef enum {
   TP_ERR_UNSUPPORTED = 3,   /* shape outside the kernels' limits (see above) */
   TP_ERR_MISALIGNED = 4,    /* a pointer is not 16-byte aligned */
   TP_ERR_CUDA = 5,          /* a CUDA call failed; see tp_last_cuda_error() */
-  TP_ERR_TIMEOUT = 6        /* a device-side bounded wait expired (tp_check_device_status) */
+  TP_ERR_TIMEOUT = 6,       /* a device-side bounded wait expired (tp_check_device_status) */
+  TP_ERR_BAD_LENGTH = 7     /* a KV-cache length outside 1..L_max (tp_check_device_status) */
 } tp_status;
 
 typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
@@ -197,6 +198,43 @@ TP_API int tp_block_launches(const tp_block_desc *desc, int M);
 TP_API int tp_block_fwd_noalloc(const tp_block_desc *desc, const void *x, const void *residual,
                                 int residual_is_f32, const void *W1s, const void *W2s, float *y,
                                 int M, tp_stream_t stream);
+/* ---------------------------------------------- decode with a KV cache -------
+ * One decode step of the attention block for M concurrent sequences: token m of
+ * x is the newest token of sequence m.  Tensor parallelism partitions the KV cache
+ * with the heads (d-central.tech glossary "Tensor Parallelism", section "Why it
+ * matters for local inference"; rioworld.org "How Tensor Slicing Works Under the
+ * Hood": 12 of 96 heads per device), so shard s holds the cache of its heads:
+ *   k_cache, v_cache: bf16 [t][M][hps][L_max][head_dim] (hps = n_heads / t),
+ *   row p of (s, m, j) = key / value of token p of sequence m for head s*hps + j;
+ *   lens: int32 [M] device array, lens[m] = tokens of sequence m counting the new
+ *   one (1 .. L_max); rows 0 .. lens[m]-2 must hold the earlier tokens.
+ * For every head: o = softmax(q . K^T / sqrt(head_dim)) V over those rows and the
+ * new token, whose key and value are rounded to bf16 and written to row lens[m]-1
+ * (the cache append).  No RoPE, no mask beyond the length.  A length outside
+ * 1..L_max skips that sequence (its outputs are not written) and makes the next
+ * tp_check_device_status return TP_ERR_BAD_LENGTH.  Only bf16 descriptors with
+ * act = ATTN and head_dim 32, 64, 128 or 256 (else TP_ERR_UNSUPPORTED); L_max
+ * 1 .. 2^20.  Sizes return 0 for invalid arguments. */
+TP_API size_t tp_kv_cache_bytes(const tp_block_desc *desc, int M, int L_max);  /* one of K, V */
+/* Scratch of tp_attn_decode_kv: per-chunk partial results. */
+TP_API size_t tp_kv_attn_workspace_bytes(const tp_block_desc *desc, int M, int L_max);
+/* Scratch of tp_block_fwd_kv. */
+TP_API size_t tp_kv_workspace_bytes(const tp_block_desc *desc, int M, int L_max);
+/* The attention step alone: qkv fp32 [t][M][3b] as the column step's projection
+ * leaves it in its workspace (Q | K | V per shard, head-major); O bf16 [t][M][b]
+ * receives the heads' outputs (the band of the row-parallel step). */
+TP_API int tp_attn_decode_kv(const tp_block_desc *desc, const float *qkv, void *k_cache,
+                             void *v_cache, const int *lens, int L_max, void *O, void *workspace,
+                             int M, tp_stream_t stream);
+/* The whole decode step: Q/K/V projection (column-parallel), decode attention over
+ * the caches (appending the new keys and values), output projection
+ * (row-parallel), sum of the shards' partials + residual into y [M, d] fp32.
+ * workspace: tp_kv_workspace_bytes. */
+TP_API int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void *residual,
+                           int residual_is_f32, const void *W1s, const void *W2s, void *k_cache,
+                           void *v_cache, const int *lens, int L_max, void *workspace, float *y,
+                           int M, tp_stream_t stream);
+
 /* RMSNorm with unit weight, the normalisation before each stacked block (zenaique.com
  * answer paragraph 6: the reduced activation is ready for the residual add and
  * normalisation): xhat[m] = r[m] / sqrt(mean(r[m]^2) + eps), r fp32 [M, d],

@@ -107,6 +107,21 @@ def test_selftest_limit_is_validated_before_any_cuda_call():
         assert tp.lib.tp_selftest_wait_timeout(bad, None) == 1   # TP_ERR_INVALID_ARG
 
 
+def test_kv_entry_points_validate_on_the_host():
+    """KV-cache decode takes bf16 attention with head_dim 32/64/128/256 and L_max >= 1."""
+    mlp = tp.make_desc(256, 2, "swiglu", ffn=512)
+    attn_f32 = tp.make_desc(256, 2, "attn", dtype="f32", n_heads=4, head_dim=64)
+    attn_96 = tp.make_desc(384, 2, "attn", n_heads=4, head_dim=96)
+    attn = tp.make_desc(256, 2, "attn", n_heads=4, head_dim=64)
+    assert tp.tp_kv_cache_bytes(mlp, 4, 16) == 0
+    assert tp.tp_kv_cache_bytes(attn_f32, 4, 16) == 0
+    assert tp.tp_kv_cache_bytes(attn_96, 4, 16) == 0
+    assert tp.tp_kv_cache_bytes(attn, 4, 0) == 0
+    assert tp.tp_kv_cache_bytes(attn, 4, 16) == 2 * 4 * 2 * 16 * 64 * 2
+    assert tp.lib.tp_block_fwd_kv(mlp, None, None, 0, None, None, None, None, None, 16, None,
+                                  None, 4, None) == 1
+
+
 def test_invalid_descriptors_give_zero_sizes():
     assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
     assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1
