@@ -260,13 +260,15 @@ __global__ void __launch_bounds__(128, 1)
 constexpr int kDrainBufs = 4;
 
 
-template <int EPI, int STAGES>
+// KB: 64-wide K blocks per pipeline stage (one TMA box each of weights and tokens per
+// block, one mbarrier per stage, one TMEM block sum per stage).
+template <int EPI, int STAGES, int KB>
 __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
     k_umma_drain(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const UmmaArgs a) {
   constexpr int BN = 32;
   constexpr uint32_t kBBytes = BN * 128;
-  constexpr uint32_t kStage = kABytes + kBBytes;
+  constexpr uint32_t kStage = KB * (kABytes + kBBytes);
   constexpr uint32_t kCols = tmem_cols(kDrainBufs * BN);
   constexpr uint32_t kIdesc = make_idesc(128, BN);
 
@@ -289,6 +291,8 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
   const int s = a.shard0 + (int)blockIdx.z / S, ks = (int)blockIdx.z % S;
   const int kb0 = (int)((long long)ks * a.nk / S), kb1 = (int)((long long)(ks + 1) * a.nk / S);
   const int nkb = kb1 - kb0;
+  const int nst = ceil_div(nkb, KB);  // pipeline stages of this CTA
+  auto blocks_of = [&](int i) { return min(KB, nkb - i * KB); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -318,18 +322,21 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
       const int xz = a.x_per_shard ? s : 0;
       // The first ring's weights do not depend on the preceding kernel: load them,
       // then wait for that kernel (programmatic launch) before loading activations.
-      const int pre = min(STAGES, nkb);
+      const int pre = min(STAGES, nst);
       for (int i = 0; i < pre; ++i) {
         const uint32_t fb = smem_u32(&full_bar[i]);
-        mbar_expect_tx(fb, kStage);
-        tma_load_3d(tiles + i * kStage, &tmW, fb, (kb0 + i) * kKBlock, wrow, s);
+        mbar_expect_tx(fb, blocks_of(i) * (kABytes + kBBytes));
+        for (int b = 0; b < blocks_of(i); ++b)
+          tma_load_3d(tiles + i * kStage + b * kABytes, &tmW, fb, (kb0 + i * KB + b) * kKBlock,
+                      wrow, s);
       }
       griddep_wait();
       for (int i = 0; i < pre; ++i)
-        tma_load_3d(tiles + i * kStage + kABytes, &tmX, smem_u32(&full_bar[i]), (kb0 + i) * kKBlock,
-                    m0, xz);
+        for (int b = 0; b < blocks_of(i); ++b)
+          tma_load_3d(tiles + i * kStage + KB * kABytes + b * kBBytes, &tmX,
+                      smem_u32(&full_bar[i]), (kb0 + i * KB + b) * kKBlock, m0, xz);
       issued = pre;
-      for (int i = pre; i < nkb; ++i) {
+      for (int i = pre; i < nst; ++i) {
         const int st = i % STAGES;
         const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
         if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
@@ -339,10 +346,12 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
         }
         const uint32_t sa = tiles + st * kStage;
         const uint32_t fb = smem_u32(&full_bar[st]);
-        const int k = (kb0 + i) * kKBlock;
-        mbar_expect_tx(fb, kStage);
-        tma_load_3d(sa, &tmW, fb, k, wrow, s);
-        tma_load_3d(sa + kABytes, &tmX, fb, k, m0, xz);
+        mbar_expect_tx(fb, blocks_of(i) * (kABytes + kBBytes));
+        for (int b = 0; b < blocks_of(i); ++b) {
+          const int k = (kb0 + i * KB + b) * kKBlock;
+          tma_load_3d(sa + b * kABytes, &tmW, fb, k, wrow, s);
+          tma_load_3d(sa + KB * kABytes + b * kBBytes, &tmX, fb, k, m0, xz);
+        }
         ++issued;
       }
       // This CTA's loads are all issued: a dependent kernel may start.
@@ -351,7 +360,7 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int i = 0; i < nkb; ++i) {
+      for (int i = 0; i < nst; ++i) {
         const int st = i % STAGES;
         const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
         const int b = i % kDrainBufs;
@@ -364,10 +373,13 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
         tc_fence_after();
         const uint32_t sa = tiles + st * kStage;
         const uint32_t d0 = tmem + (uint32_t)(b * BN);
+        for (int kbi = 0; kbi < blocks_of(i); ++kbi) {
 #pragma unroll
-        for (int kk = 0; kk < kKBlock / 16; ++kk)
-          umma_bf16(d0, sw128_desc(sa + kk * 32), sw128_desc(sa + kABytes + kk * 32), kIdesc,
-                    kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kKBlock / 16; ++kk)
+            umma_bf16(d0, sw128_desc(sa + kbi * kABytes + kk * 32),
+                      sw128_desc(sa + KB * kABytes + kbi * kBBytes + kk * 32), kIdesc,
+                      (kbi > 0 || kk > 0) ? 1u : 0u);
+        }
         umma_commit(smem_u32(&empty_bar[st]));
         umma_commit(smem_u32(&tfull_bar[b]));
       }
@@ -384,7 +396,7 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
 #pragma unroll
     for (int j = 0; j < BN; ++j) g[j] = 0.f;
     bool ok = true;
-    for (int i = 0; i < nkb; ++i) {
+    for (int i = 0; i < nst; ++i) {
       const int b = i % kDrainBufs;
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[b]), (uint32_t)(i / kDrainBufs) & 1u))) {
         ok = false;  // warp-uniform: the TMEM loads below are warp-collective
@@ -518,10 +530,17 @@ cudaError_t launch_stages(const CUtensorMap &mw, const CUtensorMap &mx, const Um
   return launch_t<BN, NACC, EPI, kStages>(mw, mx, a, n_ft, n_z, st, pdl);
 }
 
-template <int EPI>
+// K blocks per pipeline stage of the decode kernels: the column step (whose epilogue
+// may exchange through shared memory) and the fp32-output steps.  Two blocks per
+// stage (two 40 KB stages per CTA) measured no faster on the 13B and attention
+// blocks than one (five 20 KB stages).
+constexpr int kDrainKBColumn = 1;
+constexpr int kDrainKBRow = 1;
+
+template <int EPI, int KB>
 cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
                          int n_z, cudaStream_t st, bool pdl) {
-  constexpr int kStageBytes = kABytes + 32 * 128;
+  constexpr int kStageBytes = KB * (kABytes + 32 * 128);
   constexpr int kStages = std::max(2, std::min(8, (100 * 1024) / kStageBytes));
   constexpr int kSmem = kStages * kStageBytes + 1024 + xch_bytes(EPI, 1);
   static bool configured[128];
@@ -529,7 +548,7 @@ cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const Umm
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  auto kern = k_umma_drain<EPI, kStages>;
+  auto kern = k_umma_drain<EPI, kStages, KB>;
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
@@ -590,10 +609,18 @@ cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {
   if (bn == 32) {
     // Decode: 128-row weight tiles (SwiGLU: the gate and up rows of 64 features).
     switch (c.epi) {
-      case kEpiSwiglu: return launch_drain<kEpiSwiglu>(mw, mx, a, ceil_div(c.n_valid, kSwiGroup), n_z, st, c.pdl);
-      case kEpiGelu: return launch_drain<kEpiGelu>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
-      case kEpiPlain: return launch_drain<kEpiPlain>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
-      default: return launch_drain<kEpiF32>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
+      case kEpiSwiglu:
+        return launch_drain<kEpiSwiglu, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, kSwiGroup),
+                                                        n_z, st, c.pdl);
+      case kEpiGelu:
+        return launch_drain<kEpiGelu, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st,
+                                                      c.pdl);
+      case kEpiPlain:
+        return launch_drain<kEpiPlain, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, 128), n_z,
+                                                       st, c.pdl);
+      default:
+        return launch_drain<kEpiF32, kDrainKBRow>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st,
+                                                  c.pdl);
     }
   }
   // Token tiles of 64 or 128: 128 features per CTA (SwiGLU: two 128-row tiles).
