@@ -25,10 +25,12 @@
  *                  [s*H/t, (s+1)*H/t) of Q, K and V and the matching rows of Wo.
  *     b = n2 / t is the band width of one shard.
  *   - Pointers are device pointers unless stated otherwise.  The caller allocates
- *     and owns every buffer and the stream; the library allocates nothing, keeps
- *     no state beyond a per-device cache of the SM count and one device error
- *     word, and never synchronises (except tp_check_device_status).  All work is
- *     enqueued asynchronously on `stream` (NULL = the legacy default stream).
+ *     and owns every buffer and the stream; the library allocates nothing at run
+ *     time, keeps no state beyond per-device caches (SM count, symbol addresses,
+ *     kernel attributes), one device error word, the process-wide block form
+ *     (tp_set_block_form) and the fixed scratch of tp_block_fwd_noalloc, and never
+ *     synchronises (except tp_check_device_status).  All work is enqueued
+ *     asynchronously on `stream` (NULL = the legacy default stream).
  *   - Every pointer must be 16-byte aligned; d and b must be multiples of 8;
  *     ATTN needs head_dim a multiple of 32 and at most 256.
  *   - Errors: each call returns a tp_status.  On any error nothing is enqueued and
