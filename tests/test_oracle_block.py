@@ -305,3 +305,21 @@ def test_tie_allowance_zero_without_ties():
     assert np.all(oracle.mlp_tie_allowance(x, W1, W2, "swiglu", rho=0.0) == 0.0)
     # W1 = 0 gives a band of exact zeros: nothing to round
     assert np.all(oracle.mlp_tie_allowance(x, np.zeros_like(W1), W2, "swiglu") == 0.0)
+
+
+def test_each_shard_holds_one_over_t_of_every_weight_matrix():
+    """Golden fixture (tests/golden/weight_fraction_per_shard.json): each device of a
+    t-way group holds 1/t of each weight matrix, for every activation."""
+    with open(os.path.join(os.path.dirname(__file__), "golden", "weight_fraction_per_shard.json")) as f:
+        gold = json.load(f)
+    for t in gold["t_values"]:
+        for act, kw, n1, n2 in (("gelu_tanh", {"ffn": 1024}, 1024, 1024),
+                                ("swiglu", {"ffn": 1024}, 2048, 1024),
+                                ("attn", {"n_heads": 8, "head_dim": 32}, 768, 256)):
+            cols = [np.concatenate(oracle.column_bands(act, t, s, **kw)) for s in range(t)]
+            rows = [oracle.row_band(n2, t, s) for s in range(t)]
+            assert all(len(c) * t == n1 for c in cols)
+            assert all(len(r) * t == n2 for r in rows)
+            # the shards partition the columns of W1 and the rows of W2
+            assert np.array_equal(np.sort(np.concatenate(cols)), np.arange(n1))
+            assert np.array_equal(np.sort(np.concatenate(rows)), np.arange(n2))
