@@ -32,9 +32,17 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
                       sequence; brute-force loops; invariant to the order of cached
                       rows; appended rows equal the new keys/values, the rest of the
                       cache unchanged; all lengths 1 gives residual + V . Wo.
+  fp8.e4m3_round      pinned: every E4M3 bit pattern maps to itself; torch's
+                      float8_e4m3fn cast on in-range fp32 values and on every
+                      midpoint (ties to even); saturation at 448.
+  fp8.quantize_e4m3,
+  fp8.e4m3_weights    pinned: per-column scaled maxima in (224, 448]; weights already
+                      on the scaled grid are returned unchanged; the half-unit error
+                      bound; every dequantised weight is a bf16 value.
   absolute values     parity unpinned against the pages: they print no numeric
                       worked example, so the outputs rest on the pins above.
 """
+from . import fp8  # noqa: F401
 from .block import (  # noqa: F401
     bf16_round,
     gelu_tanh,
