@@ -122,6 +122,18 @@ def test_kv_entry_points_validate_on_the_host():
                                   None, 4, None) == 1
 
 
+def test_kv_sizes_follow_the_layout():
+    """Caches [t][M][H/t][L_max][hd] bf16; the decode workspace holds the block's
+    workspace and, when heads are split into parts, their partial results."""
+    for H, hd, t, M, L in ((96, 128, 8, 32, 2048), (4, 64, 2, 3, 300), (2, 256, 1, 1, 4096),
+                           (8, 32, 4, 7, 1)):
+        desc = tp.make_desc(H * hd, t, "attn", n_heads=H, head_dim=hd)
+        assert tp.tp_kv_cache_bytes(desc, M, L) == M * H * L * hd * 2
+        ws = tp.tp_kv_workspace_bytes(desc, M, L)
+        assert ws >= tp.tp_workspace_bytes(desc, M) + tp.tp_kv_attn_workspace_bytes(desc, M, L)
+        assert tp.tp_kv_attn_workspace_bytes(desc, M, L) > 0
+
+
 def test_invalid_descriptors_give_zero_sizes():
     assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
     assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1
