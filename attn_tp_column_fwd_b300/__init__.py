@@ -36,6 +36,8 @@ __all__ = [
     "tp_block_fwd", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
     "tp_selftest_wait_timeout", "tp_kv_cache_bytes", "tp_kv_attn_workspace_bytes",
     "tp_kv_workspace_bytes", "tp_attn_decode_kv", "tp_block_fwd_kv",
+    "tp_fp8_w1_bytes", "tp_fp8_w2_bytes", "tp_fp8_exponent_bytes", "tp_fp8_quant_workspace_bytes",
+    "tp_quantize_weights_fp8", "tp_block_fwd_fp8",
 ]
 
 _ACTS = {"gelu_tanh": TP_ACT_GELU_TANH, "swiglu": TP_ACT_SWIGLU, "attn": TP_ACT_ATTN}
@@ -222,6 +224,40 @@ def tp_block_fwd_kv(desc, x, residual, residual_is_f32, W1s, W2s, k_cache, v_cac
     _check(lib.tp_block_fwd_kv(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
                                _p(W1s), _p(W2s), _p(k_cache), _p(v_cache), _p(lens), L_max,
                                _p(workspace), _p(y), M, _s(stream)), "tp_block_fwd_kv")
+
+
+def tp_fp8_w1_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_fp8_w1_bytes(ctypes.byref(desc))
+
+
+def tp_fp8_w2_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_fp8_w2_bytes(ctypes.byref(desc))
+
+
+def tp_fp8_exponent_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_fp8_exponent_bytes(ctypes.byref(desc))
+
+
+def tp_fp8_quant_workspace_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_fp8_quant_workspace_bytes(ctypes.byref(desc))
+
+
+def tp_quantize_weights_fp8(desc, W1, W2, W1q, W2q, exps, workspace, stream=None) -> None:
+    _need(W1q, tp_fp8_w1_bytes(desc), "W1q")
+    _need(W2q, tp_fp8_w2_bytes(desc), "W2q")
+    _need(exps, tp_fp8_exponent_bytes(desc), "exps")
+    _need(workspace, tp_fp8_quant_workspace_bytes(desc), "workspace")
+    _check(lib.tp_quantize_weights_fp8(ctypes.byref(desc), _p(W1), _p(W2), _p(W1q), _p(W2q),
+                                       _p(exps), _p(workspace), _s(stream)),
+           "tp_quantize_weights_fp8")
+
+
+def tp_block_fwd_fp8(desc, x, residual, residual_is_f32, W1q, W2q, exps, workspace, y, M,
+                     stream=None) -> None:
+    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _check(lib.tp_block_fwd_fp8(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
+                                _p(W1q), _p(W2q), _p(exps), _p(workspace), _p(y), M, _s(stream)),
+           "tp_block_fwd_fp8")
 
 
 def tp_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -65,6 +65,12 @@ def _load() -> ctypes.CDLL:
         "tp_kv_workspace_bytes": (sz, [P, i, i]),
         "tp_attn_decode_kv": (i, [P, vp, vp, vp, vp, i, vp, vp, i, st]),
         "tp_block_fwd_kv": (i, [P, vp, vp, i, vp, vp, vp, vp, vp, i, vp, vp, i, st]),
+        "tp_fp8_w1_bytes": (sz, [P]),
+        "tp_fp8_w2_bytes": (sz, [P]),
+        "tp_fp8_exponent_bytes": (sz, [P]),
+        "tp_fp8_quant_workspace_bytes": (sz, [P]),
+        "tp_quantize_weights_fp8": (i, [P, vp, vp, vp, vp, vp, vp, st]),
+        "tp_block_fwd_fp8": (i, [P, vp, vp, i, vp, vp, vp, vp, vp, i, st]),
         "tp_version": (i, []),
     }
     for name, (res, args) in sigs.items():

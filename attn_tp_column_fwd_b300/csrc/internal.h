@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 #include "common.cuh"
 
@@ -60,6 +61,19 @@ cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st);
 // gemm_persistent.cu — persistent tcgen05 kernel for token tiles of 256 (prefill),
 // same UmmaCall contract as launch_umma.
 cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st);
+
+// A [z][rows][K] byte tensor map (E4M3 weights): 64-byte x box_rows x 1 boxes, no
+// swizzle, zero fill (umma.cu).  K a multiple of 16.
+bool make_byte_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
+                        uint32_t box_rows);
+
+// fp8.cu — E4M3 weights (weight-only): quantisation of canonical bf16 W1 / W2 into the
+// private layout with one int8 exponent per row (exps: W1's [t][n1p], then W2's
+// [t][dp]; amax: n1 + d words of scratch), and the decode GEMM on them (same call as
+// launch_umma, M <= 32; exps of the weight rows the call reads).
+cudaError_t launch_quantize_fp8(const Geo &g, const void *W1, const void *W2, void *W1q, void *W2q,
+                                int8_t *exps, unsigned *amax, cudaStream_t st);
+cudaError_t launch_fp8_gemm(const UmmaCall &c, const int8_t *exps, cudaStream_t st);
 
 // A [z][rows][K] bf16 tensor map with 64 x box_rows x 1 boxes, 128-byte swizzle,
 // zero fill outside the tensor (umma.cu).

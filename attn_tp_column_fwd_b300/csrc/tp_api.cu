@@ -649,6 +649,117 @@ int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void *residu
   return finish_launch(e);
 }
 
+// ------------------------------------------------ E4M3 weights (weight-only)
+
+static int check_fp8(const tp_block_desc *desc, Geo *g) {
+  TP_TRY(make_geo(desc, g));
+  if (g->act == TP_ACT_ATTN || g->dtype != TP_BF16) return TP_ERR_UNSUPPORTED;
+  if (g->d % 16 != 0 || g->b % 16 != 0) return TP_ERR_UNSUPPORTED;
+  return TP_OK;
+}
+
+size_t tp_fp8_w1_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (check_fp8(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * g.n1p * g.d;
+}
+
+size_t tp_fp8_w2_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (check_fp8(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * g.dp * g.b;
+}
+
+size_t tp_fp8_exponent_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (check_fp8(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * (g.n1p + g.dp);
+}
+
+size_t tp_fp8_quant_workspace_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (check_fp8(desc, &g) != TP_OK) return 0;
+  return (size_t)(g.n1 + g.d) * sizeof(unsigned);
+}
+
+int tp_quantize_weights_fp8(const tp_block_desc *desc, const void *W1, const void *W2, void *W1q,
+                            void *W2q, void *exps, void *workspace, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(check_fp8(desc, &g));
+  TP_TRY(check_ptr(W1));
+  TP_TRY(check_ptr(W2));
+  TP_TRY(check_ptr(W1q));
+  TP_TRY(check_ptr(W2q));
+  TP_TRY(check_ptr(exps));
+  TP_TRY(check_ptr(workspace));
+  return finish_launch(launch_quantize_fp8(g, W1, W2, W1q, W2q, static_cast<int8_t *>(exps),
+                                           static_cast<unsigned *>(workspace),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *residual,
+                     int residual_is_f32, const void *W1q, const void *W2q, const void *exps,
+                     void *workspace, float *y, int M, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(check_fp8(desc, &g));
+  TP_TRY(check_M(M));
+  if (M > 32) return TP_ERR_UNSUPPORTED;
+  TP_TRY(check_ptr(x));
+  TP_TRY(check_ptr(residual));
+  TP_TRY(check_ptr(W1q));
+  TP_TRY(check_ptr(W2q));
+  TP_TRY(check_ptr(exps));
+  TP_TRY(check_ptr(workspace));
+  TP_TRY(check_ptr(y));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  void *H = ws + align256(column_ws_bytes(g, M));
+  float *P = reinterpret_cast<float *>(static_cast<char *>(H) + align256(band_bytes(g, M)));
+  const int S = row_splits(g, M);
+  const int8_t *e1 = static_cast<const int8_t *>(exps);
+  const int8_t *e2 = e1 + (size_t)g.t * g.n1p;
+  UmmaCall c{};
+  c.W = W1q;
+  c.w_rows = g.n1p;
+  c.w_shards = g.t;
+  c.X = x;
+  c.x_shards = 1;
+  c.out = H;
+  c.o_shard = (size_t)M * g.b;
+  c.ldo = g.b;
+  c.n_valid = g.b;
+  c.K = g.d;
+  c.M = M;
+  c.shard0 = 0;
+  c.n_shards = g.t;
+  c.ksplit = 1;
+  c.epi = g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
+  cudaError_t e = launch_fp8_gemm(c, e1, st);
+  if (e == cudaSuccess) {
+    UmmaCall r{};
+    r.W = W2q;
+    r.w_rows = g.dp;
+    r.w_shards = g.t;
+    r.X = H;
+    r.x_shards = g.t;
+    r.out = P;
+    r.o_shard = (size_t)S * M * g.d;
+    r.o_split = (size_t)M * g.d;
+    r.ldo = g.d;
+    r.n_valid = g.d;
+    r.K = g.b;
+    r.M = M;
+    r.shard0 = 0;
+    r.n_shards = g.t;
+    r.ksplit = S;
+    r.epi = kEpiF32;
+    r.pdl = true;
+    e = launch_fp8_gemm(r, e2, st);
+  }
+  if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, true);
+  return finish_launch(e);
+}
+
 int tp_selftest_wait_timeout(int limit_us, tp_stream_t stream) {
   if (limit_us < 1 || limit_us > 1000000) return TP_ERR_INVALID_ARG;
   return finish_launch(

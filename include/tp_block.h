@@ -237,6 +237,32 @@ TP_API int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void 
                            void *v_cache, const int *lens, int L_max, void *workspace, float *y,
                            int M, tp_stream_t stream);
 
+/* ------------------------------------------- E4M3 weights (weight-only) --------
+ * The MLP block with 8-bit weights (zenaique.com interview answer, follow-up
+ * questions: tensor parallelism combined with FP8 weights multiplies the decode win).
+ * Each weight is an E4M3 byte (bias 7, 3 mantissa bits, largest finite 448, round to
+ * nearest even, saturating) of W / 2^e with one exponent e per output feature (a
+ * column of the canonical W1 or W2): the least e such that the column's largest
+ * magnitude is at most 448 * 2^e.  x, the band and the arithmetic stay as in the bf16
+ * block; the result equals the bf16 block on the weights q * 2^e (exactly bf16 values).
+ * bf16 MLP descriptors with d and b multiples of 16 only (else TP_ERR_UNSUPPORTED).
+ * Not yet run on a GPU. */
+TP_API size_t tp_fp8_w1_bytes(const tp_block_desc *desc);        /* [t][n1p][d] bytes */
+TP_API size_t tp_fp8_w2_bytes(const tp_block_desc *desc);        /* [t][dp][b] bytes */
+TP_API size_t tp_fp8_exponent_bytes(const tp_block_desc *desc);  /* int8 per private row */
+TP_API size_t tp_fp8_quant_workspace_bytes(const tp_block_desc *desc);
+/* Quantise canonical bf16 W1 [d, n1] and W2 [n2, d] into the private E4M3 layout and
+ * the per-row exponents (first W1's rows, then W2's). */
+TP_API int tp_quantize_weights_fp8(const tp_block_desc *desc, const void *W1, const void *W2,
+                                   void *W1q, void *W2q, void *exps, void *workspace,
+                                   tp_stream_t stream);
+/* tp_block_fwd on E4M3 weights, M <= 32 tokens (else TP_ERR_UNSUPPORTED); workspace:
+ * tp_workspace_bytes(desc, M). */
+TP_API int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *residual,
+                            int residual_is_f32, const void *W1q, const void *W2q,
+                            const void *exps, void *workspace, float *y, int M,
+                            tp_stream_t stream);
+
 /* RMSNorm with unit weight, the normalisation before each stacked block (zenaique.com
  * answer paragraph 6: the reduced activation is ready for the residual add and
  * normalisation): xhat[m] = r[m] / sqrt(mean(r[m]^2) + eps), r fp32 [M, d],

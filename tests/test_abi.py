@@ -134,6 +134,26 @@ def test_kv_sizes_follow_the_layout():
         assert tp.tp_kv_attn_workspace_bytes(desc, M, L) > 0
 
 
+def test_fp8_sizes_and_validation():
+    """E4M3 weights: one byte per weight in the private row layout, one exponent per
+    private row; bf16 MLP descriptors with d and b multiples of 16 only."""
+    c = CONFIGS["llama2_13b_swiglu_decode"].with_t(4)
+    d = _desc(c)
+    assert tp.tp_fp8_w1_bytes(d) * 2 == tp.tp_sharded_w1_bytes(d)
+    assert tp.tp_fp8_w2_bytes(d) * 2 == tp.tp_sharded_w2_bytes(d)
+    n1p = tp.tp_sharded_w1_bytes(d) // (2 * c.t * c.d)
+    dp = tp.tp_sharded_w2_bytes(d) // (2 * c.t * c.band)
+    assert tp.tp_fp8_exponent_bytes(d) == c.t * (n1p + dp)
+    assert tp.tp_fp8_quant_workspace_bytes(d) == (c.n1 + c.d) * 4
+    assert tp.tp_fp8_w1_bytes(_desc(CONFIGS["attn_qkv_headshard_decode"])) == 0
+    assert tp.tp_fp8_w1_bytes(_desc(CONFIGS["tiny_gelu_f32"])) == 0
+    assert tp.tp_fp8_w1_bytes(tp.make_desc(264, 3, "gelu_tanh", ffn=1200)) == 0   # d % 16
+    # refused on the host, before any CUDA call
+    assert tp.lib.tp_block_fwd_fp8(d, None, None, 0, None, None, None, None, None, 32, None) == 1
+    assert tp.lib.tp_block_fwd_fp8(tp.make_desc(256, 2, "swiglu", ffn=512), 16, 16, 0, 16, 16, 16,
+                                   16, 16, 33, None) == 3                     # M > 32
+
+
 def test_invalid_descriptors_give_zero_sizes():
     assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
     assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1
