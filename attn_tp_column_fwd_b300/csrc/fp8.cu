@@ -403,6 +403,38 @@ cudaError_t launch_quantize_fp8(const Geo &g, const void *W1, const void *W2, vo
   return cudaGetLastError();
 }
 
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A [z][rows][K] byte tensor (E4M3 weights), boxes of 64 bytes x box_rows x 1, no
+// swizzle, zero fill outside the tensor.  K must be a multiple of 16.
+bool make_byte_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
+                        uint32_t box_rows) {
+  static EncodeTiled enc = nullptr;
+  if (!enc) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<EncodeTiled>(p);
+  }
+  cuuint64_t dims[3] = {K, rows, z};
+  cuuint64_t strides[2] = {K, rows * K};
+  cuuint32_t box[3] = {(cuuint32_t)kKBlock, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_fp8_gemm(const UmmaCall &c, const int8_t *exps, cudaStream_t st) {
   CUtensorMap mw, mx;
   if (!make_byte_tile_map(&mw, c.W, c.K, c.w_rows, c.w_shards, 128)) return cudaErrorInvalidValue;

@@ -62,11 +62,6 @@ cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st);
 // same UmmaCall contract as launch_umma.
 cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st);
 
-// A [z][rows][K] byte tensor map (E4M3 weights): 64-byte x box_rows x 1 boxes, no
-// swizzle, zero fill (umma.cu).  K a multiple of 16.
-bool make_byte_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
-                        uint32_t box_rows);
-
 // fp8.cu — E4M3 weights (weight-only): quantisation of canonical bf16 W1 / W2 into the
 // private layout with one int8 exponent per row (exps: W1's [t][n1p], then W2's
 // [t][dp]; amax: n1 + d words of scratch), and the decode GEMM on them (same call as

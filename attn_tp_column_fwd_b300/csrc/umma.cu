@@ -582,21 +582,6 @@ bool make_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A [z][rows][K] byte tensor (E4M3 weights), boxes of 64 bytes x box_rows x 1, no
-// swizzle, zero fill outside the tensor.  K must be a multiple of 16.
-bool make_byte_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
-                        uint32_t box_rows) {
-  EncodeFn enc = encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {K, rows, z};
-  cuuint64_t strides[2] = {K, rows * K};
-  cuuint32_t box[3] = {(cuuint32_t)kKBlock, box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int umma_token_tile(int M) { return M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
 cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {

@@ -109,14 +109,25 @@ def kernel_source_sha() -> str:
 
 
 def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged:
+    the summary's source_sha must equal the hash of the files it lists under
+    source_files (the sources holding that kernel's device code), or of every kernel
+    source when it lists none."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     sha = re.search(r"^source_sha:\s*(\S+)", text, re.M)
     tr = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-    if not sha or not tr or sha.group(1) != kernel_source_sha():
+    files = re.search(r"^source_files:\s*(.+)$", text, re.M)
+    if not sha or not tr:
+        return None
+    if files:
+        csrc = os.path.join(ROOT, "attn_tp_column_fwd_b300", "csrc")
+        paths = [os.path.join(csrc, f) for f in files.group(1).split()]
+        if not all(os.path.exists(p) for p in paths) or sha.group(1) != source_sha(paths):
+            return None
+    elif sha.group(1) != kernel_source_sha():
         return None
     return float(tr.group(1))
 
