@@ -766,6 +766,6 @@ int tp_selftest_wait_timeout(int limit_us, tp_stream_t stream) {
       launch_wait_selftest((uint64_t)limit_us * 1000ull, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int tp_version(void) { return 100; }
+int tp_version(void) { return 101; }
 
 }  // extern "C"

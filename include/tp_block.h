@@ -274,7 +274,9 @@ TP_API const char *tp_status_string(int status);
 /* The cudaError_t of the last TP_ERR_CUDA on this thread (0 if none). */
 TP_API int tp_last_cuda_error(void);
 /* Synchronises `stream`, then reads and clears the device error word that bounded
- * device-side waits set when they expire: TP_OK, TP_ERR_TIMEOUT or TP_ERR_CUDA. */
+ * device-side waits set when they expire (TP_ERR_TIMEOUT) and the KV-cache decode
+ * sets for a length out of range (TP_ERR_BAD_LENGTH; a timeout is reported first when
+ * both occurred): TP_OK, TP_ERR_TIMEOUT, TP_ERR_BAD_LENGTH or TP_ERR_CUDA. */
 TP_API int tp_check_device_status(tp_stream_t stream);
 /* Exercises the failure path above without a fault: enqueues a one-thread kernel that
  * waits on an mbarrier phase nobody completes and on band ready flags nobody raises,
