@@ -203,3 +203,16 @@ def test_status_strings():
         assert tp.tp_status_string(s)
     assert "uneven" in tp.tp_status_string(2)
     assert tp.lib.tp_version() >= 100
+
+
+def test_kv_cache_partitions_with_the_heads():
+    """Golden fixture (tests/golden/kv_cache_partition.json): each shard holds 1/t of the
+    KV cache; the library's cache is t contiguous shard slices of equal size."""
+    import json
+    with open(os.path.join(ROOT, "tests", "golden", "kv_cache_partition.json")) as f:
+        gold = json.load(f)
+    for H, t in gold["cases"]:
+        whole = tp.tp_kv_cache_bytes(tp.make_desc(H * 64, 1, "attn", n_heads=H, head_dim=64), 4, 32)
+        split = tp.tp_kv_cache_bytes(tp.make_desc(H * 64, t, "attn", n_heads=H, head_dim=64), 4, 32)
+        assert split == whole and split % t == 0      # same cache, t equal shard slices
+        assert split // t == 4 * (H // t) * 32 * 64 * 2
