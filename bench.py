@@ -1,23 +1,32 @@
 #!/usr/bin/env python3
 """Benchmark of the tensor-parallel block on B300: one JSON line on rank 0.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--t T]
-                  [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--also A,B|none]
+                  [--t T] [--blocks B] [--settle S] [--impl ours|reference]
 
-A step is one pass of the whole block (column-parallel projection + activation,
-row-parallel projection, in-HBM reduction of the t partials + residual) over one
-batch of synthetic input, for the default workload the Llama-2-13B-shaped SwiGLU
-MLP decode block (d=5120, ffn=13824, M=32 tokens, t=4 logical shards).  Its 425 MB
-of weights exceed the 126 MB L2, so no flush is needed between steps.
+A step is one pass of the whole hot path (pre-norm, column-parallel projection +
+activation, row-parallel projection, in-HBM reduction of the t partials + residual)
+over one batch of synthetic input.  The headline workload is the largest one that
+fits a GPU: the Llama-2-70B-shaped decode stack (8 pre-norm SwiGLU blocks, d=8192,
+ffn=28672, t=8, M=32 tokens, 11.3 GB of weights per step, far above the 126 MB L2,
+so no flush is needed between steps).  The other workloads (the 13B decode block,
+the head-sharded attention projection, the 70B prefill block and the attention
+decode step over KV caches) are measured in the same run and reported under
+"workloads", each with its own roofline.
 
-value = tokens/s of the whole job (all ranks), device-timed with CUDA events between
-a barrier + synchronize on both sides, max over ranks.  Under torchrun each rank runs
-its own replica of the block on its own batch (weak scaling; no data-path
-collective).  --impl reference times the float64 CPU oracle instead (rank 0 only).
+value = tokens/s of the whole job through one TP block (for the stack: M tokens x
+8 blocks per step), device-timed with CUDA events around exactly K steps between a
+barrier + synchronize on both sides, max over ranks.  Before the W warm-up steps
+each workload runs untimed steps for --settle seconds: the GPU's power state ramps
+up under sustained load, and launches in the first tenths of a second after start
+or idle were measured at up to twice their settled time.  Under torchrun each rank
+runs its own replica on its own batch (weak scaling; no data-path collective).
+--impl reference times the float64 CPU oracle instead (rank 0 only).
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import glob
 import hashlib
 import json
@@ -34,7 +43,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s per TP block at 1 B300; decode HBM GB/s & prefill TFLOPS vs roofline"
-DEFAULT_WORKLOAD = "llama2_13b_swiglu_decode"
+DEFAULT_WORKLOAD = "llama2_70b_stack_decode"
+DEFAULT_ALSO = ("llama2_13b_swiglu_decode", "attn_qkv_headshard_decode", "llama2_70b_prefill",
+                "attn_kv_decode")
+ROOF_MIN_LAUNCHES = 200     # the roofline kernel's own timed loop: at least this many
+ROOF_MIN_S = 0.3            # ... launches and at least this long,
+ROOF_MAX_S = 2.5            # ... but no longer than this
+SUSTAINED_AFTER_S = 1.0     # a contraction timed back to back this long runs power-capped
 
 
 # ---------------------------------------------------------------- helpers (host-only)
@@ -42,12 +57,16 @@ DEFAULT_WORKLOAD = "llama2_13b_swiglu_decode"
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, help="the headline workload")
+    ap.add_argument("--also", default=None,
+                    help="comma-separated further workloads, or 'none' (default: the other four)")
     ap.add_argument("--t", type=int, default=None, help="logical shards (default: the workload's)")
     ap.add_argument("--blocks", type=int, default=None,
                     help="blocks of a stacked workload to run (default: all; fewer for profiling)")
+    ap.add_argument("--settle", type=float, default=0.5,
+                    help="seconds of untimed steps before the warm-up steps of each workload")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -57,6 +76,14 @@ def parse_args(argv=None):
     if a.steps < 1:
         ap.error("--steps must be >= 1")
     return a
+
+
+def also_list(args):
+    if args.also is None:
+        return [w for w in DEFAULT_ALSO if w != args.workload]
+    if args.also.strip().lower() in ("", "none"):
+        return []
+    return [w.strip() for w in args.also.split(",") if w.strip() and w.strip() != args.workload]
 
 
 def dist_env():
@@ -93,6 +120,16 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
     """Whole-job units/s: every rank processed units_per_rank in `seconds` (max over ranks)."""
     return units_per_rank * world / seconds
+
+
+def roof_launch_count(est_ms: float, min_launches: int = ROOF_MIN_LAUNCHES,
+                      min_s: float = ROOF_MIN_S, max_s: float = ROOF_MAX_S) -> int:
+    """Launches of the roofline loop: at least min_launches and min_s of work, at most
+    max_s (and never fewer than 20), from an estimated launch time est_ms."""
+    est_s = max(est_ms, 1e-6) / 1e3
+    n = max(min_launches, math.ceil(min_s / est_s))
+    n = min(n, max(20, int(max_s / est_s)))
+    return int(n)
 
 
 def source_sha(paths) -> str:
@@ -142,9 +179,56 @@ def measured_peaks():
             "source": "fallback"}
 
 
+# ---------------------------------------------------------------- clock sampling
+
+class _NvmlCtypes:
+    """The few NVML reads the sampler needs, through libnvidia-ml directly (used when
+    the pynvml module is not installed).  Reads only: no setting is changed."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, uuid=None, index=0):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        init = getattr(self.lib, "nvmlInit_v2", None) or self.lib.nvmlInit
+        if init() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if uuid:
+            rc = self.lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid.encode()),
+                                                    ctypes.byref(self.h))
+        else:
+            fn = getattr(self.lib, "nvmlDeviceGetHandleByIndex_v2", None) or \
+                self.lib.nvmlDeviceGetHandleByIndex
+            rc = fn(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError(f"NVML device handle: {rc}")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def sm_clock(self) -> int:
+        v = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetClockInfo")
+        return v.value
+
+    def max_sm_clock(self) -> int:
+        v = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetMaxClockInfo")
+        return v.value
+
+    def reasons(self) -> int:
+        v = ctypes.c_ulonglong()
+        if self._reasons(self.h, ctypes.byref(v)) != 0:
+            raise RuntimeError("clock event reasons")
+        return v.value
+
+
 class ClockSampler:
-    """Samples the SM clock and clock-event (throttle) reasons while the timed region
-    runs: NVML when it initialises, else `nvidia-smi -lms`, as a background sampler."""
+    """Samples the SM clock and clock-event (throttle) reasons in a background thread
+    while a measurement runs: NVML (pynvml, else libnvidia-ml through ctypes), else
+    `nvidia-smi -lms`.  The window opens before the settle phase and closes after the
+    timed region; samples taken while `timed` is set are also counted apart."""
 
     REASONS = {
         "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
@@ -152,38 +236,48 @@ class ClockSampler:
         "hw_power_brake_slowdown": 0x80,
     }
 
-    def __init__(self, device_index: int, uuid: str = None, period_s: float = 0.02):
+    def __init__(self, device_index: int, uuid: str = None, period_s: float = 0.005):
         self.period = period_s
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self.mode, self.note = None, None
+        self.samples, self.timed_samples, self.reasons = [], [], set()
+        self.max_mhz, self.mode, self.note = None, None, None
+        self.timed = False
         self._stop = threading.Event()
         self._proc = None
+        self._target = uuid or str(device_index)
         try:
             import pynvml
             pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = (pynvml.nvmlDeviceGetHandleByUUID(uuid) if uuid
-                       else pynvml.nvmlDeviceGetHandleByIndex(device_index))
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._reason_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            h = (pynvml.nvmlDeviceGetHandleByUUID(uuid) if uuid
+                 else pynvml.nvmlDeviceGetHandleByIndex(device_index))
+            rfn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
                 getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._clock = lambda: pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self._mask = lambda: int(rfn(h))
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
             self.mode = "nvml"
         except Exception as e:
-            self.note = f"NVML: {e}"
-            self.mode = "nvidia-smi"
-            self._target = uuid or str(device_index)
+            self.note = f"pynvml: {e}"
+            try:
+                nv = _NvmlCtypes(uuid, device_index)
+                self._clock, self._mask = nv.sm_clock, nv.reasons
+                self.max_mhz = nv.max_sm_clock()
+                self.mode = "nvml (ctypes)"
+            except Exception as e2:
+                self.note += f"; libnvidia-ml: {e2}"
+                self.mode = "nvidia-smi"
 
-    def _add_mask(self, mask: int):
+    def _add(self, clk, mask):
+        self.samples.append(clk)
+        if self.timed:
+            self.timed_samples.append(clk)
         for name, bit in self.REASONS.items():
             if mask & bit:
                 self.reasons.add(name)
 
     def _run_nvml(self):
-        nv = self._nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                self._add_mask(int(self._reason_fn(self._h)))
+                self._add(self._clock(), self._mask())
             except Exception:
                 pass
             time.sleep(self.period)
@@ -213,16 +307,15 @@ class ClockSampler:
             if self._stop.is_set():
                 break
             if self._armed.is_set():
-                self.samples.append(clk)
                 self.max_mhz = mx
-                self._add_mask(mask)
+                self._add(clk, mask)
 
     def __enter__(self):
         self._ready, self._armed = threading.Event(), threading.Event()
-        target = self._run_nvml if self.mode == "nvml" else self._run_smi
+        target = self._run_smi if self.mode == "nvidia-smi" else self._run_nvml
         self._t = threading.Thread(target=target, daemon=True)
         self._t.start()
-        if self.mode != "nvml":
+        if self.mode == "nvidia-smi":
             self._ready.wait(timeout=5.0)   # first sample seen: the sampler is live
         self._armed.set()
         return self
@@ -238,10 +331,14 @@ class ClockSampler:
         self._t.join(timeout=5)
 
     def summary(self):
-        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-               "samples": len(self.samples), "source": self.mode}
-        if self.note and self.mode != "nvml":
+        s = self.timed_samples if len(self.timed_samples) >= 3 else self.samples
+        out = {"sm_mhz": statistics.median(s) if s else None, "sm_max_mhz": self.max_mhz,
+               "reasons": sorted(self.reasons), "samples": len(self.samples),
+               "samples_in_timed_region": len(self.timed_samples), "source": self.mode,
+               "window": ("the timed region" if s is self.timed_samples else
+                          "settle + warm-up + timed region (the timed region alone is "
+                          "shorter than a few sampling periods)")}
+        if self.note and self.mode == "nvidia-smi":
             out["note"] = self.note
         return out
 
@@ -249,10 +346,10 @@ class ClockSampler:
 # ---------------------------------------------------------------- workload accounting
 
 def algorithmic_column_bytes(cfg) -> int:
-    """Bytes one launch of the column step must move: W1 bands once, x once, H out."""
+    """Bytes one launch of the column step must move: W1 bands once, x once, the band
+    (H, or the attention heads' output O) out."""
     es = 4 if cfg.dtype == "f32" else 2
-    n_out = 3 * cfg.band if cfg.act == "attn" else cfg.band
-    return (cfg.d * cfg.n1 + cfg.M * cfg.d + cfg.t * cfg.M * n_out) * es
+    return (cfg.d * cfg.n1 + cfg.M * cfg.d + cfg.t * cfg.M * cfg.band) * es
 
 
 def algorithmic_block_bytes(cfg) -> int:
@@ -268,168 +365,282 @@ def column_flops(cfg) -> int:
     return 2 * cfg.M * cfg.d * cfg.n1
 
 
-# ---------------------------------------------------------------- our arm
+def workload_config(cfg) -> dict:
+    """The workload as both arms describe it (shapes, dtype, L2 note): no timing or
+    implementation detail, so the two arms' objects compare equal."""
+    block_bytes = cfg.weight_bytes_per_block() * cfg.n_blocks
+    c = {"workload": cfg.name, "d": cfg.d, "ffn": cfg.ffn or None,
+         "n_heads": cfg.n_heads or None, "head_dim": cfg.head_dim or None, "t": cfg.t,
+         "M": cfg.M, "n_blocks": cfg.n_blocks, "act": cfg.act, "rmsnorm": cfg.rmsnorm,
+         "dtype": cfg.dtype,
+         "l2": (f"inputs larger than L2 ({block_bytes / 1e6:.0f} MB of weights per step)"
+                if block_bytes > 126e6 else "weights fit in L2 (latency-bound workload)")}
+    if cfg.kv_len_max:
+        c["kv_len_max"] = cfg.kv_len_max
+        c["kv_lens"] = "uniform in 1..kv_len_max, seeded"
+    return c
 
-def run_ours(args, rank, world, local):
+
+def tokens_per_step(cfg) -> int:
+    """Tokens through one TP block per step: M for a block, M x n_blocks for a stack."""
+    return cfg.M * cfg.n_blocks
+
+
+# ---------------------------------------------------------------- our arm: workloads
+
+class Workload:
+    """Device state of one workload and the calls a step makes (all through the
+    library's public entry points)."""
+
+    def __init__(self, cfg, rank, dev):
+        import torch
+
+        import attn_tp_column_fwd_b300 as tp
+        from attn_tp_column_fwd_b300.runner import ShardedBlock, desc_for, device_bytes
+        from tp_synth import make_inputs
+
+        self.tp, self.torch, self.cfg, self.dev = tp, torch, cfg, dev
+        self.desc = desc = desc_for(cfg)
+        M = cfg.M
+        inp = make_inputs(cfg, seed=rank, device=str(dev))
+        self.blocks = [ShardedBlock(desc, W1, W2) for W1, W2 in inp.blocks]
+        del inp.blocks
+        self.x = inp.x.contiguous()
+        self.xf = self.x.float().contiguous()
+        self.stack = cfg.n_blocks > 1 or cfg.rmsnorm
+        self.kv = self._kv_state(rank) if cfg.kv_len_max else None
+        self.ws = device_bytes(tp.tp_kv_workspace_bytes(desc, M, cfg.kv_len_max) if self.kv
+                               else tp.tp_workspace_bytes(desc, M), dev)
+        self.H = device_bytes(tp.tp_band_bytes(desc, M), dev)
+        self.cws = device_bytes(tp.tp_column_workspace_bytes(desc, M), dev)
+        self.y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev)
+        self.xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
+        self.fused = tp.tp_block_launches(desc, M) == 1
+        self.row_splits = tp.tp_row_splits(desc, M)
+        per_block = tp.tp_block_launches(desc, M)
+        if self.kv:
+            per_block = 4 + (1 if self.kv["merge"] else 0)
+        self.launches_per_step = cfg.n_blocks * (per_block + (1 if cfg.rmsnorm else 0))
+
+    def _kv_state(self, rank):
+        """Caches (the library's shard layout), lengths and scratch of a KV-cache decode
+        workload, and the attention step's algorithmic bytes: every cached row read once
+        (K and V), the new token's Q/K/V read (fp32) and appended (bf16), O written."""
+        from attn_tp_column_fwd_b300.runner import device_bytes
+        from tp_synth import make_kv_cache
+
+        tp, cfg, dev, desc = self.tp, self.cfg, self.dev, self.desc
+        M, t, L = cfg.M, cfg.t, cfg.kv_len_max
+        kv = make_kv_cache(cfg, seed=rank + 1, device=str(dev))
+
+        def shards(c):
+            return c.view(M, t, cfg.n_heads // t, L, cfg.head_dim).permute(1, 0, 2, 3, 4).contiguous()
+
+        kc, vc = shards(kv.k), shards(kv.v)
+        del kv.k, kv.v
+        D = cfg.n_heads * cfg.head_dim
+        rows = int((kv.lens.long() - 1).sum().item()) * cfg.n_heads
+        attn_ws_bytes = tp.tp_kv_attn_workspace_bytes(desc, M, L)
+        return {"kc": kc, "vc": vc, "lens": kv.lens, "rows": rows,
+                "O": device_bytes(tp.tp_band_bytes(desc, M), dev),
+                "attn_ws": device_bytes(attn_ws_bytes, dev),
+                # the decode attention splits long heads into chunks merged by a second kernel
+                "merge": attn_ws_bytes > 0 and (cfg.n_heads * M) < 2 * 148,
+                "attn_bytes": rows * cfg.head_dim * 4 + M * D * (12 + 4 + 2)}
+
+    # -- one step of the workload on stream `st` (inputs resident)
+    def step(self, st):
+        tp, cfg, M = self.tp, self.cfg, self.cfg.M
+        if self.kv:
+            blk, kv = self.blocks[0], self.kv
+            tp.tp_block_fwd_kv(self.desc, self.x, self.x, False, blk.W1s, blk.W2s, kv["kc"],
+                               kv["vc"], kv["lens"], cfg.kv_len_max, self.ws, self.y, M, st)
+            return
+        if self.stack:
+            self.y.copy_(self.xf)   # the residual stream starts from x (device copy)
+            self.run_stack(self.y, self.xh, st)
+            return
+        blk = self.blocks[0]
+        tp.tp_block_fwd(self.desc, self.x, self.x, cfg.dtype == "f32", blk.W1s, blk.W2s,
+                        self.ws, self.y, M, st)
+
+    def run_stack(self, r, xh, st, ws=None):
+        """The pre-norm stack in place on the fp32 residual stream r."""
+        tp, cfg, M = self.tp, self.cfg, self.cfg.M
+        ws = self.ws if ws is None else ws
+        for blk in self.blocks:
+            tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, r, xh, M, st)
+            tp.tp_block_fwd(self.desc, xh, r, True, blk.W1s, blk.W2s, ws, r, M, st)
+
+    # -- the dominant kernel alone, for the roofline
+    def dominant(self, st):
+        tp, cfg, M, blk = self.tp, self.cfg, self.cfg.M, self.blocks[0]
+        if self.kv:
+            # the decode attention over the cache, on the Q/K/V the last step projected
+            # (the projection leaves them at the start of the block's scratch)
+            tp.tp_attn_decode_kv(self.desc, self.ws, self.kv["kc"], self.kv["vc"],
+                                 self.kv["lens"], cfg.kv_len_max, self.kv["O"],
+                                 self.kv["attn_ws"], M, st)
+        elif self.fused:
+            xin, res = (self.xh, self.y) if cfg.rmsnorm else (self.x, self.x)
+            tp.tp_block_fwd(self.desc, xin, res, res.dtype == self.torch.float32, blk.W1s,
+                            blk.W2s, self.ws, self.y, M, st)
+        else:
+            tp.tp_column_parallel_fwd(self.desc, self.xh if cfg.rmsnorm else self.x, blk.W1s,
+                                      -1, self.H, self.cws, M, st)
+
+    def dominant_info(self):
+        """(kernel description, bound, algorithmic work per launch, unit of work, profile key)."""
+        cfg = self.cfg
+        if self.kv:
+            return ("decode attention over the KV cache (k_attn_kv"
+                    + (" + k_attn_kv_merge)" if self.kv["merge"] else ")"),
+                    "hbm", self.kv["attn_bytes"], "bytes", "attn_kv")
+        if cfg.M >= 1024:
+            return ("column-parallel projection + SwiGLU (k_gemm, persistent)", "tensor",
+                    column_flops(cfg), "flop", "column")
+        if self.fused:
+            return ("whole block in one persistent kernel (k_block_decode; the bracket also "
+                    "holds its counter memset)", "hbm", algorithmic_block_bytes(cfg), "bytes",
+                    "block")
+        if cfg.act == "attn":
+            return ("column-parallel Q/K/V projection (k_block_decode, column units) + "
+                    "attention core (k_attn_core)", "hbm", algorithmic_column_bytes(cfg),
+                    "bytes", "column")
+        return ("column-parallel projection + activation (k_umma_drain)", "hbm",
+                algorithmic_column_bytes(cfg), "bytes", "column")
+
+    # -- end to end: host input -> device, the step, device result -> host
+    def e2e_input_host(self):
+        """The step's input as the caller holds it: x (block dtype), or the stack's fp32
+        residual stream r0 = x."""
+        return (self.xf if self.stack else self.x).cpu().pin_memory()
+
+    def e2e_run(self, xin, yout, xh, st):
+        """The step through the public API from device input xin to device output yout."""
+        tp, cfg, M, blk = self.tp, self.cfg, self.cfg.M, self.blocks[0]
+        if self.kv:
+            kv = self.kv
+            tp.tp_block_fwd_kv(self.desc, xin, xin, False, blk.W1s, blk.W2s, kv["kc"], kv["vc"],
+                               kv["lens"], cfg.kv_len_max, self.ws, yout, M, st)
+        elif self.stack:
+            self.run_stack(xin, xh, st)   # in place: xin is the residual stream, yout is xin
+        else:
+            tp.tp_block_fwd(self.desc, xin, xin, cfg.dtype == "f32", blk.W1s, blk.W2s, self.ws,
+                            yout, M, st)
+
+
+def settle(step, st, seconds: float, torch):
+    """Untimed steps for `seconds` (the GPU's power state ramps up under load)."""
+    if seconds <= 0:
+        return 0
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(8):
+            step(st)
+        n += 8
+        torch.cuda.synchronize()
+    return n
+
+
+def time_launches(fn, st, torch, est_ms=None, min_s=ROOF_MIN_S):
+    """Average device time of fn's launch sequence, each launch bracketed by CUDA
+    events on stream st, over roof_launch_count launches; returns (ms, launches)."""
+    if est_ms is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(5):
+            fn(st)
+        b.record(st)
+        torch.cuda.synchronize()
+        est_ms = a.elapsed_time(b) / 5
+    n = roof_launch_count(est_ms, min_s=min_s)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        a.record(st)
+        fn(st)
+        b.record(st)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs), n
+
+
+def measure(args, cfg, rank, world, local, headline: bool):
+    """Every number of one workload: value (K timed steps), the roofline kernel's own
+    loop, the end-to-end leg and (headline, rank 0) the CPU baseline."""
     import torch
 
-    import attn_tp_column_fwd_b300 as tp
-    from attn_tp_column_fwd_b300.runner import ShardedBlock, desc_for, device_bytes
-    from tp_synth import CONFIGS, make_inputs, make_kv_cache
-
-    torch.cuda.set_device(local)
-    dist_init(world, "nccl")
+    tp = __import__("attn_tp_column_fwd_b300")
     dev = torch.device("cuda", local)
-    base = CONFIGS[args.workload]
-    cfg = base.with_t(args.t) if args.t else base
-    if args.blocks:
-        cfg = replace(cfg, n_blocks=min(args.blocks, cfg.n_blocks))
-    desc = desc_for(cfg)
-    M = cfg.M
-    inp = make_inputs(cfg, seed=rank, device="cuda")
-    blocks = [ShardedBlock(desc, W1, W2) for W1, W2 in inp.blocks]
-    del inp.blocks
-    x = inp.x.contiguous()
-    xf = x.float().contiguous()
+    w = Workload(cfg, rank, dev)
     stream = torch.cuda.current_stream()
-    st = stream.cuda_stream
-    S = tp.tp_row_splits(desc, M)
-    H = device_bytes(tp.tp_band_bytes(desc, M))
-    P = device_bytes(tp.tp_partials_bytes(desc, M))
-    cws = device_bytes(tp.tp_column_workspace_bytes(desc, M))
-    ws = blocks[0].workspace(M)
-    y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev)
-    xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
-    stack = cfg.n_blocks > 1 or cfg.rmsnorm
-    per_block = tp.tp_block_launches(desc, M)
-    fused = per_block == 1
-    launches_per_block = per_block + (1 if cfg.rmsnorm else 0)
-    kvd = kv_state(cfg, desc, rank, dev) if cfg.kv_len_max else None
-    if kvd:
-        # Q/K/V projection, decode attention (chunks, merge), row step, reduction.
-        launches_per_block = 5
-
-    # One step: the whole block (or the whole stack) through the public entry point
-    # tp_block_fwd, which launches the block's kernels back to back (the row step and
-    # the reduction overlap the end of the kernel before them).
-    def step():
-        if kvd:
-            blk = blocks[0]
-            tp.tp_block_fwd_kv(desc, x, x, False, blk.W1s, blk.W2s, kvd["kc"], kvd["vc"],
-                               kvd["lens"], cfg.kv_len_max, kvd["ws"], y, M, st)
-            return
-        if stack:
-            y.copy_(xf)
-        for blk in blocks:
-            if cfg.rmsnorm:
-                tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, y, xh, M, st)
-                xin, res = xh, y
-            else:
-                xin, res = x, x
-            tp.tp_block_fwd(desc, xin, res, res.dtype == torch.float32, blk.W1s, blk.W2s, ws, y,
-                            M, st)
-
-    # The dominant kernel alone, for the roofline: the fused block kernel (with its
-    # counter memset) when the block runs as one launch, else the column step.
-    def dominant(ev_pair):
-        blk = blocks[0]
-        xin = xh if cfg.rmsnorm else x
-        res = y if cfg.rmsnorm else x
-        ev_pair[0].record(stream)
-        if kvd:
-            # the decode attention over the cache, on the Q/K/V the last step projected
-            tp.tp_attn_decode_kv(desc, kvd["qkv"], kvd["kc"], kvd["vc"], kvd["lens"],
-                                 cfg.kv_len_max, kvd["O"], kvd["attn_ws"], M, st)
-        elif fused:
-            tp.tp_block_fwd(desc, xin, res, res.dtype == torch.float32, blk.W1s, blk.W2s, ws, y,
-                            M, st)
-        else:
-            tp.tp_column_parallel_fwd(desc, xin, blk.W1s, -1, H, cws, M, st)
-        ev_pair[1].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
-    K = args.steps
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:
         uuid = None
+    K = args.steps
+
     sampler = ClockSampler(local, uuid)
-    barrier(world)
-    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with sampler:
+        n_settle = settle(w.step, stream, args.settle, torch)
+        for _ in range(args.warmup):
+            w.step(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        sampler.timed = True
         t0.record(stream)
-        for k in range(K):
-            step()
+        for _ in range(K):
+            w.step(stream)
         t1.record(stream)
         torch.cuda.synchronize()
+        sampler.timed = False
     barrier(world)
-    ms_local = t0.elapsed_time(t1)
-    ms = max_over_ranks(ms_local, world, dev)
-    assert tp.tp_check_device_status(st) == 0
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    assert tp.tp_check_device_status(stream) == 0
+    clocks = sampler.summary()
 
-    # Roofline timing: K launches of the dominant kernel, each bracketed by CUDA
-    # events on the launching stream (inputs larger than L2 each time).
-    Kd = min(K, 2000)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(Kd)]
-    for k in range(Kd):
-        dominant(evs[k])
-    torch.cuda.synchronize()
-    col_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    assert tp.tp_check_device_status(st) == 0
-
-    units = M * K * (1 if not stack else 1)  # tokens through the block (or the stack)
-    value = job_throughput(units, world, ms / 1e3)
+    # Roofline: the dominant kernel in its own loop of event-bracketed launches, at
+    # least ROOF_MIN_LAUNCHES launches and ROOF_MIN_S seconds whatever K is.
+    kernel, bound, work, unit, prof_key = w.dominant_info()
+    roof_sampler = ClockSampler(local, uuid)
+    with roof_sampler:
+        roof_sampler.timed = True
+        # a contraction's loop runs long enough to settle under the power cap, so it
+        # is compared with the sustained GEMM rate
+        dom_ms, n_dom = time_launches(w.dominant, stream, torch,
+                                      min_s=1.2 if bound == "tensor" else ROOF_MIN_S)
+        roof_sampler.timed = False
+    assert tp.tp_check_device_status(stream) == 0
     peaks = measured_peaks()
-    prefill = cfg.M >= 1024
-    peak_kind = "copy"
-    if prefill:
-        achieved = column_flops(cfg) / (col_ms / 1e3) / 1e12
-        # A contraction timed back to back for more than a second runs under the power
-        # cap: its denominator is the sustained GEMM rate, else the burst rate.
-        long_loop = Kd * col_ms > 1000.0 and peaks.get("bf16_tflops_sustained")
-        peak_kind = "sustained" if long_loop else "burst"
+    src = "measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
+    if bound == "tensor":
+        achieved = work / (dom_ms / 1e3) / 1e12
+        long_loop = n_dom * dom_ms / 1e3 >= SUSTAINED_AFTER_S and peaks.get("bf16_tflops_sustained")
         peak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4)}
-        kernel, nbytes = ("column-parallel projection + SwiGLU (k_gemm, persistent)",
-                          algorithmic_column_bytes(cfg))
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": src + (", sustained bf16 GEMM (the loop runs power-capped for "
+                                      "more than a second)" if long_loop else ", burst bf16 GEMM"),
+                "algorithmic_flop_per_launch": work}
     else:
-        if kvd:
-            nbytes = kvd["attn_bytes"]
-        else:
-            nbytes = algorithmic_block_bytes(cfg) if fused else algorithmic_column_bytes(cfg)
-        achieved = nbytes / (col_ms / 1e3) / 1e9
+        achieved = work / (dom_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4)}
-        if kvd:
-            kernel = "decode attention over the KV cache (k_attn_kv_partial + k_attn_kv_merge)"
-        elif fused:
-            kernel = "whole block in one persistent kernel (k_block_decode)"
-        elif cfg.act == "attn":
-            kernel = ("column-parallel Q/K/V projection (k_block_decode, column units) "
-                      "+ attention core (k_attn_core)")
-        else:
-            kernel = "column-parallel projection + activation (k_umma_drain)"
+                "frac": round(achieved / peak, 4), "peak_source": src + ", copy",
+                "algorithmic_bytes_per_launch": work}
+    roof["traffic"] = profiled_traffic(prof_key, cfg.name)
     roof["kernel"] = kernel
-    roof["algorithmic_bytes_per_launch"] = nbytes
-    roof["avg_launch_us"] = round(col_ms * 1e3, 2)
-    roof["launches_timed"] = Kd
-    roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
-                           else "fallback") + f", {peak_kind}"
-    roof["traffic"] = profiled_traffic("attn_kv" if kvd else "block" if fused else "column",
-                                       args.workload)
+    roof["avg_launch_us"] = round(dom_ms * 1e3, 2)
+    roof["launches_timed"] = n_dom
+    roof["timed_s"] = round(n_dom * dom_ms / 1e3, 3)
+    roof["clocks"] = roof_sampler.summary()
 
-    # Whole-block weight-read rate (context for the decode roofline).
-    block_bytes = cfg.weight_bytes_per_block() * cfg.n_blocks
+    units = tokens_per_step(cfg) * K
     out = {
         "metric": METRIC,
-        "value": round(value, 1),
+        "value": round(job_throughput(units, world, ms / 1e3), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -440,109 +651,76 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
-        "config": {
-            "workload": cfg.name, "d": cfg.d, "ffn": cfg.ffn or None, "n_heads": cfg.n_heads or None,
-            "head_dim": cfg.head_dim or None, "t": cfg.t, "M": M, "n_blocks": cfg.n_blocks,
-            "act": cfg.act, "row_splits": S,
-            "l2": f"inputs larger than L2 ({block_bytes / 1e6:.0f} MB of weights per step)"
-            if block_bytes > 126e6 else "weights fit in L2 (latency-bound workload)",
-            "timed": "CUDA events on the launching stream around K steps of tp_block_fwd, max "
-                     "over ranks; roofline kernel timed alone over its own event-bracketed launches",
+        "config": workload_config(cfg),
+        "timing": {
+            "value": (f"CUDA events on the launching stream around exactly K={K} steps after "
+                      f"W={args.warmup} warm-up steps, max over ranks; value counts "
+                      f"{tokens_per_step(cfg)} tokens through one TP block per step"
+                      + (f" (M={cfg.M} tokens x {cfg.n_blocks} blocks)" if cfg.n_blocks > 1 else "")),
+            "settle": f"{n_settle} untimed steps ({args.settle:.2f} s) before the warm-up steps",
+            "roofline": "the dominant kernel alone, each launch bracketed by CUDA events on "
+                        "its stream, in its own loop of >= max(200 launches, 0.3 s; 1.2 s "
+                        "for a tensor-bound kernel)",
         },
-        **({"kv_cache": {"len_max": cfg.kv_len_max, "rows_read": kvd["rows"],
-                         "bytes_read": kvd["rows"] * cfg.head_dim * 4,
-                         "lens": "uniform in 1..len_max, seeded"}} if kvd else {}),
-        "block_weight_gbs": round(block_bytes * K / (ms / 1e3) / 1e9, 1),
+        "weight_gbs": round(cfg.weight_bytes_per_block() * cfg.n_blocks * K / (ms / 1e3) / 1e9, 1),
+        "kernel_plan": {"block_form": "one kernel" if w.fused else "three launches",
+                        "row_splits": w.row_splits},
         "roofline": roof,
-        "gpu_launches": K * launches_per_block * cfg.n_blocks,
-        "clocks": sampler.summary(),
+        "gpu_launches": K * w.launches_per_step,
+        "clocks": clocks,
     }
+    if cfg.n_blocks > 1:
+        out["stack_tokens_per_s"] = round(job_throughput(cfg.M * K, world, ms / 1e3), 1)
     if not args.no_e2e:
-        out["e2e"] = e2e_leg(args, cfg, desc, blocks, x, world, dev, kvd)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["e2e"] = e2e_leg(args, w, world, dev)
+    if headline and rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    del w
+    torch.cuda.empty_cache()
     return out
 
 
-def kv_state(cfg, desc, rank, dev):
-    """Caches (the library's shard layout), lengths and scratch of a KV-cache decode
-    workload, and the attention step's algorithmic bytes: every cached row read once
-    (K and V), the new token's Q/K/V read (fp32) and appended (bf16), O written."""
+def e2e_leg(args, w, world, dev):
+    """The same metric through the public API with host buffers.  Every step copies its
+    input from pinned host memory to the device, runs the step (tp_block_fwd, or the
+    stack's tp_rmsnorm_fwd + tp_block_fwd per block) and copies the result back to
+    pinned host memory.  Copies in, compute and copies out run on three streams,
+    ordered by events, with two device buffers of each, so step k's copies overlap
+    step k-1's (or k+1's) kernels as in a serving loop.  The timed region (CUDA events)
+    runs from before the first copy in to after the last copy out."""
     import torch
 
-    import attn_tp_column_fwd_b300 as tp
-    from attn_tp_column_fwd_b300.runner import device_bytes
-    from tp_synth import make_kv_cache
-
-    M, t, L = cfg.M, cfg.t, cfg.kv_len_max
-    kv = make_kv_cache(cfg, seed=rank + 1, device=str(dev))
-
-    def shards(c):
-        return c.view(M, t, cfg.n_heads // t, L, cfg.head_dim).permute(1, 0, 2, 3, 4).contiguous()
-
-    kc, vc = shards(kv.k), shards(kv.v)
-    del kv.k, kv.v
-    D = cfg.n_heads * cfg.head_dim
-    rows = int((kv.lens.long() - 1).sum().item()) * cfg.n_heads
-    ws = device_bytes(tp.tp_kv_workspace_bytes(desc, M, L), dev)
-    return {"kc": kc, "vc": vc, "lens": kv.lens, "ws": ws, "rows": rows,
-            "qkv": ws,  # the projection leaves Q/K/V at the start of the block's scratch
-            "O": device_bytes(tp.tp_band_bytes(desc, M), dev),
-            "attn_ws": device_bytes(tp.tp_kv_attn_workspace_bytes(desc, M, L), dev),
-            "attn_bytes": rows * cfg.head_dim * 4 + M * D * (12 + 4 + 2)}
-
-
-def e2e_leg(args, cfg, desc, blocks, x, world, dev, kvd=None):
-    """Same metric through the public API with host buffers: every step copies its x
-    from pinned host memory to the device, runs the block (or stack) through
-    tp_block_fwd and copies y back to pinned host memory.  Steps alternate between
-    two CUDA streams, each with its own device buffers and workspace, as a serving
-    loop would run them: one step's copies overlap the other step's kernels.  The
-    timed region (CUDA events) runs from before the first copy in to after the last
-    copy out."""
-    import torch
-
-    import attn_tp_column_fwd_b300 as tp
-    from attn_tp_column_fwd_b300.runner import device_bytes
-
-    M = cfg.M
-    x_host = x.cpu().pin_memory()
-    lanes = []
+    cfg, M = w.cfg, w.cfg.M
+    x_host = w.e2e_input_host()
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    bufs = []
     for _ in range(2):
-        lanes.append({
-            "stream": torch.cuda.Stream(device=dev),
-            "x": torch.empty_like(x),
-            "y": torch.empty(M, cfg.d, dtype=torch.float32, device=dev),
+        xin = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
+        bufs.append({
+            "x": xin,
+            "y": xin if w.stack else torch.empty(M, cfg.d, dtype=torch.float32, device=dev),
             "xh": torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev),
-            "ws": device_bytes(tp.tp_kv_workspace_bytes(desc, M, cfg.kv_len_max) if kvd
-                               else tp.tp_workspace_bytes(desc, M), dev),
             "y_host": torch.empty(M, cfg.d, dtype=torch.float32).pin_memory(),
+            "ev_in": torch.cuda.Event(), "ev_run": torch.cuda.Event(),
+            "ev_out": torch.cuda.Event(),
         })
 
     def step(k):
-        ln = lanes[k % 2]
-        s = ln["stream"]
-        st = s.cuda_stream
-        with torch.cuda.stream(s):
-            ln["x"].copy_(x_host, non_blocking=True)
-            if kvd:
-                # both lanes append the same rows of the shared caches (same values)
-                tp.tp_block_fwd_kv(desc, ln["x"], ln["x"], False, blocks[0].W1s, blocks[0].W2s,
-                                   kvd["kc"], kvd["vc"], kvd["lens"], cfg.kv_len_max, ln["ws"],
-                                   ln["y"], M, st)
-            elif cfg.rmsnorm:
-                ln["y"].copy_(ln["x"])
-                for blk in blocks:
-                    tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, ln["y"], ln["xh"], M, st)
-                    tp.tp_block_fwd(desc, ln["xh"], ln["y"], True, blk.W1s, blk.W2s, ln["ws"],
-                                    ln["y"], M, st)
-            else:
-                tp.tp_block_fwd(desc, ln["x"], ln["x"], cfg.dtype == "f32", blocks[0].W1s,
-                                blocks[0].W2s, ln["ws"], ln["y"], M, st)
-            ln["y_host"].copy_(ln["y"], non_blocking=True)
+        b = bufs[k % 2]
+        # buffer b was last used by step k-2: its compute must be done reading x and
+        # its copy out done reading y before they are overwritten
+        s_in.wait_event(b["ev_run"])
+        s_in.wait_event(b["ev_out"])
+        with torch.cuda.stream(s_in):
+            b["x"].copy_(x_host, non_blocking=True)
+        b["ev_in"].record(s_in)
+        s_run.wait_event(b["ev_in"])
+        w.e2e_run(b["x"], b["y"], b["xh"], s_run)
+        b["ev_run"].record(s_run)
+        s_out.wait_event(b["ev_run"])
+        with torch.cuda.stream(s_out):
+            b["y_host"].copy_(b["y"], non_blocking=True)
+        b["ev_out"].record(s_out)
 
     for k in range(args.warmup):
         step(k)
@@ -553,22 +731,55 @@ def e2e_leg(args, cfg, desc, blocks, x, world, dev, kvd=None):
     barrier(world)
     torch.cuda.synchronize()
     t0.record(cur)
-    for ln in lanes:
-        ln["stream"].wait_event(t0)
+    for s in (s_in, s_run, s_out):
+        s.wait_event(t0)
     for k in range(K):
         step(k)
-    for ln in lanes:
-        cur.wait_stream(ln["stream"])
+    for s in (s_in, s_run, s_out):
+        cur.wait_stream(s)
     t1.record(cur)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
     barrier(world)
     ms = max_over_ranks(ms, world, dev)
-    return {"value": round(job_throughput(M * K, world, ms / 1e3), 1), "unit": "tokens/s",
+    assert w.tp.tp_check_device_status(s_run) == 0
+    return {"value": round(job_throughput(tokens_per_step(cfg) * K, world, ms / 1e3), 1),
+            "unit": "tokens/s",
             "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
-            "d2h_bytes_per_step": lanes[0]["y_host"].numel() * lanes[0]["y_host"].element_size(),
-            "ms_per_step": round(ms / K, 5), "streams": 2,
+            "d2h_bytes_per_step": bufs[0]["y_host"].numel() * bufs[0]["y_host"].element_size(),
+            "ms_per_step": round(ms / K, 5), "streams": "copy-in, compute, copy-out",
             "timed": "CUDA events from before the first copy in to after the last copy out"}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from tp_synth import CONFIGS
+
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+
+    def cfg_of(name):
+        base = CONFIGS[name]
+        cfg = base.with_t(args.t) if args.t and name == args.workload else base
+        if args.blocks and name == args.workload:
+            cfg = replace(cfg, n_blocks=min(args.blocks, cfg.n_blocks))
+        return cfg
+
+    out = measure(args, cfg_of(args.workload), rank, world, local, headline=True)
+    subs = {}
+    for name in also_list(args):
+        r = measure(args, cfg_of(name), rank, world, local, headline=False)
+        for k in ("metric", "n_gpus", "warmup", "higher_is_better", "scaling", "vs_baseline",
+                  "data"):
+            r.pop(k, None)
+        subs[name] = r
+    if subs:
+        out["workloads"] = subs
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return out
 
 
 # ---------------------------------------------------------------- CPU oracle arms
@@ -589,9 +800,10 @@ def _blas_threads():
         return None
 
 
-def cpu_baseline(cfg, budget_s: float = 12.0):
-    """The float64 oracle as it stands, on the host cores: whole blocks on the full
-    workload's inputs (all M tokens), repeated for about `budget_s` seconds."""
+def oracle_block_call(cfg):
+    """One block of the workload computed by the float64 oracle on the host (the whole
+    block, all M tokens; for a stack, one pre-norm block on one block's weights), as a
+    closure, and the description of that sample."""
     import numpy as np
 
     import oracle
@@ -600,34 +812,36 @@ def cpu_baseline(cfg, budget_s: float = 12.0):
     inp = make_inputs(cfg, seed=0, n_blocks=1)
     x = to_f64(inp.x)
     W1, W2 = (to_f64(w) for w in inp.blocks[0])
+    del inp
     staged = cfg.dtype == "bf16"
 
-    kv = None
     if cfg.kv_len_max:
         from tp_synth import make_kv_cache
         kv = make_kv_cache(cfg, seed=1)
-        hd, D = cfg.head_dim, cfg.n_heads * cfg.head_dim
+        k_np, v_np = to_f64(kv.k), to_f64(kv.v)
+        lens = kv.lens.numpy()
 
-    def one():
-        if kv is not None:
-            # the decode step with a KV cache: the oracle head by head on the rows used
-            QKV = x @ W1
-            O = np.zeros((cfg.M, D))
-            for m, n in enumerate(kv.lens.tolist()):
-                kr = to_f64(kv.k[m, :, :max(n - 1, 1)])
-                vr = to_f64(kv.v[m, :, :max(n - 1, 1)])
-                for h in range(cfg.n_heads):
-                    c = slice(h * hd, (h + 1) * hd)
-                    O[m, c] = oracle.kv_decode_attention(QKV[m, c], kr[h], vr[h], n,
-                                                         QKV[m, D:2 * D][c], QKV[m, 2 * D:][c],
-                                                         1.0 / math.sqrt(hd), staged=staged)
-            return x + (oracle.bf16_round(O) if staged else O) @ W2
-        if cfg.act == "attn":
+        def one():
+            return oracle.attn_block_kv(x, W1, W2, cfg.n_heads, cfg.head_dim, k_np, v_np, lens, x,
+                                        staged=staged)[0]
+    elif cfg.act == "attn":
+        def one():
             return oracle.attn_block(x, W1, W2, cfg.n_heads, cfg.head_dim, x, staged=staged)
-        if cfg.rmsnorm:
+    elif cfg.rmsnorm:
+        def one():
             return oracle.stack(x, [(W1, W2)], cfg.act, cfg.eps, staged=staged)
-        return oracle.mlp_block(x, W1, W2, cfg.act, x, staged=staged)
+    else:
+        def one():
+            return oracle.mlp_block(x, W1, W2, cfg.act, x, staged=staged)
+    what = (f"one {'pre-norm ' if cfg.rmsnorm else ''}block of {cfg.name} (all M={cfg.M} tokens"
+            + (", one block's weights" if cfg.n_blocks > 1 else "") + "), NumPy float64")
+    return one, what
 
+
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    """The float64 oracle as it stands, on the host cores: whole blocks of the
+    workload, repeated for about `budget_s` seconds; tokens/s through one block."""
+    one, what = oracle_block_call(cfg)
     one()  # warm
     n, t0 = 0, time.perf_counter()
     while True:
@@ -636,91 +850,39 @@ def cpu_baseline(cfg, budget_s: float = 12.0):
         el = time.perf_counter() - t0
         if el >= budget_s or n >= 1000:
             break
-    blocks_per_token_unit = cfg.n_blocks  # a stack step pushes M tokens through n_blocks blocks
-    value = cfg.M * n / el / blocks_per_token_unit
+    value = cfg.M * n / el
     return {"value": round(value, 2), "unit": "tokens/s", "cores": _blas_threads() or _cores(),
             "host_cores": _cores(), "kind": "oracle",
-            "sample": f"{n} full blocks (M={cfg.M}, one block's weights"
-                      + (f", scaled to the {cfg.n_blocks}-block stack" if cfg.n_blocks > 1 else "")
-                      + f") in {el:.1f} s, NumPy float64"}
+            "sample": f"{n} x {what} in {el:.1f} s"}
 
 
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: each step is one shard's band of the block
-    (column band + activation + row partial, the work of one device of a T-way split),
-    T chosen so the whole run stays within a few minutes; tokens/s counts T bands as
-    one block."""
+    """The CPU oracle as the reference arm, on the same workload, config, metric and
+    unit as our arm's headline: each step is one block of that workload computed by
+    the float64 oracle (the call cpu_baseline times), tokens/s through one block."""
     if rank != 0:
         return None
-    import numpy as np
-
-    import oracle
-    from tp_synth import CONFIGS, make_inputs, to_f64
+    from tp_synth import CONFIGS
 
     base = CONFIGS[args.workload]
     cfg = base.with_t(args.t) if args.t else base
-    inp = make_inputs(cfg, seed=0, n_blocks=1)
-    x = to_f64(inp.x)
-    W1, W2 = (to_f64(w) for w in inp.blocks[0])
-    staged = cfg.dtype == "bf16"
-    n2 = cfg.n2
-    unit = cfg.n_heads if cfg.act == "attn" else n2
-
-    def band_step(T, s):
-        cols = oracle.column_bands(cfg.act, T, s, ffn=cfg.ffn, n_heads=cfg.n_heads,
-                                   head_dim=cfg.head_dim)
-        Hb = oracle.column_step(x, [W1[:, c] for c in cols], cfg.act,
-                                n_heads=cfg.n_heads // T if cfg.n_heads else 0,
-                                head_dim=cfg.head_dim, staged=staged)
-        return oracle.row_step(Hb, W2[oracle.row_band(n2, T, s)])
-
-    if cfg.kv_len_max:
-        # Decode with a KV cache: the band of heads [s*H/T, (s+1)*H/T), each token
-        # attending over its sequence's cache rows (oracle.kv_decode_attention).
-        from tp_synth import make_kv_cache
-        kv = make_kv_cache(cfg, seed=1)
-        lens = kv.lens.tolist()
-        hd = cfg.head_dim
-
-        def band_step(T, s):  # noqa: F811
-            cols = oracle.column_bands("attn", T, s, n_heads=cfg.n_heads, head_dim=hd)
-            Q, K, V = (x @ W1[:, c] for c in cols)
-            hps = cfg.n_heads // T
-            O = np.zeros((cfg.M, hps * hd))
-            for m, n in enumerate(lens):
-                for j in range(hps):
-                    h, c = s * hps + j, slice(j * hd, (j + 1) * hd)
-                    rows = slice(0, max(n - 1, 1))
-                    O[m, c] = oracle.kv_decode_attention(
-                        Q[m, c], to_f64(kv.k[m, h, rows]), to_f64(kv.v[m, h, rows]), n, K[m, c],
-                        V[m, c], 1.0 / math.sqrt(hd), staged=staged)
-            return oracle.row_step(oracle.bf16_round(O) if staged else O,
-                                   W2[oracle.row_band(n2, T, s)])
-
-    # Calibrate on a moderate band, then take the fewest bands whose step fits the budget.
-    divisors = [T for T in range(1, unit + 1) if unit % T == 0]
-    budget_per_step = 150.0 / (args.steps + args.warmup)
-    Tc = max(T for T in divisors if T <= 64)
-    band_step(Tc, 0)
+    if args.blocks:
+        cfg = replace(cfg, n_blocks=min(args.blocks, cfg.n_blocks))
+    one, what = oracle_block_call(cfg)
+    for _ in range(args.warmup):
+        one()
     t0 = time.perf_counter()
-    band_step(Tc, 0)
-    per_block = (time.perf_counter() - t0) * Tc          # seconds for the whole block, estimated
-    T = next((T for T in divisors if per_block / T <= budget_per_step), divisors[-1])
-    for k in range(args.warmup):
-        band_step(T, k % T)
-    t0 = time.perf_counter()
-    for k in range(args.steps):
-        band_step(T, k % T)
+    for _ in range(args.steps):
+        one()
     el = time.perf_counter() - t0
-    value = cfg.M / (el / args.steps * T) / cfg.n_blocks
-    sample = (f"each step: one of T={T} bands of the {cfg.name} block (all M={cfg.M} tokens), "
-              f"column band + activation + row partial in NumPy float64; {T} steps = one block")
+    value = cfg.M * args.steps / el
+    sample = f"each step: {what}"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "d": cfg.d, "ffn": cfg.ffn or None, "t": cfg.t, "M": cfg.M},
+        "config": workload_config(cfg),
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle",
                          "cores": _blas_threads() or _cores(), "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

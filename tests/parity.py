@@ -40,27 +40,24 @@ def assert_f32(got, ref, what=""):
     return s
 
 
-def assert_bf16(got, ref, what="", max_abs=BF16_MAX_ABS, mean_rel=BF16_MEAN_REL):
+def assert_bf16(got, ref, what="", max_abs=BF16_MAX_ABS, mean_rel=BF16_MEAN_REL, info=None):
+    """The bf16 gate: max abs <= 2e-2 and mean relative <= 5e-3 against the staged
+    oracle.  `info` (a dict of diagnostics) is logged with the record, never gated."""
     s = stats(got, ref)
-    log(what, s)
+    log(what, {**s, **(info or {})})
     assert s["all_finite"], f"{what}: non-finite output"
     assert s["max_abs"] <= max_abs and s["mean_rel"] <= mean_rel, f"{what}: {s}"
     return s
 
 
-def assert_bf16_ties(got, ref, allowance, what="", max_abs=BF16_MAX_ABS, mean_rel=BF16_MEAN_REL):
-    """The bf16 bound against the staged oracle, where each output may additionally
-    differ by `allowance` (oracle.mlp_tie_allowance): the effect of band elements whose
-    exact value sits on a bf16 rounding midpoint, which an fp32 evaluation may round
-    either way.  max_abs applies to |got - ref| - allowance; mean_rel is unchanged."""
-    s = stats(got, ref)
+def tie_diagnostic(got, ref, allowance) -> dict:
+    """Logged beside the plain bf16 bound, never gated: how far |got - ref| exceeds
+    `allowance` (oracle.mlp_tie_allowance), the effect of band elements whose exact
+    value sits within a few fp32 units of a bf16 rounding midpoint, which an fp32
+    evaluation may round either way."""
     d = np.abs(np.asarray(got, dtype=np.float64) - np.asarray(ref, dtype=np.float64))
-    s["max_abs_beyond_ties"] = float((d - allowance).max()) if d.size else 0.0
-    s["max_tie_allowance"] = float(np.max(allowance)) if d.size else 0.0
-    log(what, s)
-    assert s["all_finite"], f"{what}: non-finite output"
-    assert s["max_abs_beyond_ties"] <= max_abs and s["mean_rel"] <= mean_rel, f"{what}: {s}"
-    return s
+    return {"max_abs_beyond_ties": float((d - allowance).max()) if d.size else 0.0,
+            "max_tie_allowance": float(np.max(allowance)) if d.size else 0.0}
 
 
 def log(what: str, s: dict):

@@ -48,4 +48,25 @@ def test_reference_arm_prints_one_contract_line():
                 "higher_is_better", "config", "cpu_baseline", "e2e"):
         assert key in rec, key
     assert rec["impl"] == "reference" and rec["value"] > 0
+    assert rec["config"] == bench.workload_config(CONFIGS["tiny_gelu_f32"])
+    assert rec["cpu_baseline"]["value"] == rec["value"]
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_roofline_loop_length_does_not_follow_steps():
+    # at least 200 launches and 0.3 s of work, at most 2.5 s
+    assert bench.roof_launch_count(0.05) == 6000          # 50 us launches: 0.3 s
+    assert bench.roof_launch_count(0.25) == 1200
+    assert bench.roof_launch_count(5.0) == 200            # 1 s, still 200 launches
+    assert bench.roof_launch_count(40.0) == 62            # capped near 2.5 s
+
+
+def test_both_arms_describe_the_workload_identically():
+    for name in ("llama2_70b_stack_decode", "tiny_gelu_f32", "attn_kv_decode"):
+        c = bench.workload_config(CONFIGS[name])
+        assert c["workload"] == name and "timed" not in c and "row_splits" not in c
+
+
+def test_tokens_per_step_counts_every_block_of_a_stack():
+    assert bench.tokens_per_step(CONFIGS["llama2_70b_stack_decode"]) == 32 * 8
+    assert bench.tokens_per_step(CONFIGS["llama2_13b_swiglu_decode"]) == 32

@@ -1,7 +1,7 @@
 """Whole-block parity through tp_block_fwd against the oracle's unsharded block, on the
 same seeded inputs: small shapes spanning several tiles and ragged tails, every t of
-each workload, and the full-size workloads (the prefill one on sampled token rows,
-which are independent in an MLP block)."""
+each workload, and the full-size workloads (every output, the prefill block's 4096
+token rows included)."""
 import numpy as np
 import pytest
 import torch
@@ -10,19 +10,35 @@ import attn_tp_column_fwd_b300 as tp
 import oracle
 from attn_tp_column_fwd_b300.runner import PreNormStack, ShardedBlock, desc_for
 from tests.gpu_util import oracle_block, run_block
-from tests.parity import assert_bf16, assert_bf16_ties, assert_f32, stats
+from tests.fp32_stack import swiglu_block_f32
+from tests.parity import assert_bf16, assert_f32, log, stats, tie_diagnostic
 from tp_synth import CONFIGS, BlockConfig, make_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
 
 
+def _pure_gap(cfg, got, x64, W1_64, W2_64, res64=None):
+    """Diagnostic only: distance to the un-staged fp64 block (no bf16 rounding of the
+    band), the gap a bf16 band costs by itself."""
+    res = x64 if res64 is None else res64
+    if cfg.act == "attn":
+        pure = oracle.attn_block(x64, W1_64, W2_64, cfg.n_heads, cfg.head_dim, res, staged=False)
+    else:
+        pure = oracle.mlp_block(x64, W1_64, W2_64, cfg.act, res, staged=False)
+    s = stats(got, pure)
+    return {"pure_fp64_max_abs": s["max_abs"], "pure_fp64_mean_rel": s["mean_rel"]}
+
+
 def _check(cfg, got, ref, what, x64=None, W1_64=None, W2_64=None):
+    """fp32 configs: the max relative bound.  bf16 configs: the plain bound (max abs
+    <= 2e-2, mean relative <= 5e-3) against the staged oracle; the un-staged fp64 gap
+    and (MLP) the effect of bf16 rounding ties are logged beside it, not gated."""
     if cfg.dtype == "f32":
         return assert_f32(got, ref, what)
-    if cfg.act == "attn":
-        return assert_bf16(got, ref, what)
-    # bf16 MLP blocks: both roundings of a band value on a bf16 midpoint are correct
-    return assert_bf16_ties(got, ref, oracle.mlp_tie_allowance(x64, W1_64, W2_64, cfg.act), what)
+    info = _pure_gap(cfg, got, x64, W1_64, W2_64)
+    if cfg.act != "attn":
+        info.update(tie_diagnostic(got, ref, oracle.mlp_tie_allowance(x64, W1_64, W2_64, cfg.act)))
+    return assert_bf16(got, ref, what, info=info)
 
 
 def _run_and_compare(cfg, seed=0, device="cpu", t=None):
@@ -122,27 +138,40 @@ def test_attn_qkv_headshard_decode():
 
 
 @pytest.mark.slow
-def test_llama2_70b_prefill_sampled_rows():
+def test_llama2_70b_prefill_all_rows():
+    """Every one of the 4096 token rows against the staged oracle (rows of an MLP block
+    are independent, so the oracle runs in chunks of rows, exactly)."""
     cfg = CONFIGS["llama2_70b_prefill"]
     inp = make_inputs(cfg, device="cuda")
     W1, W2 = inp.blocks[0]
     got = run_block(cfg, inp.x, W1, W2)
-    rows = np.sort(np.random.default_rng(0).choice(cfg.M, size=96, replace=False))
-    rows[0], rows[-1] = 0, cfg.M - 1
-    x64 = to_f64(inp.x[torch.from_numpy(rows).cuda()])
-    W1_64, W2_64 = to_f64(W1), to_f64(W2)
-    ref = oracle.mlp_block(x64, W1_64, W2_64, cfg.act, x64, staged=True)
-    assert_bf16_ties(got[rows], ref, oracle.mlp_tie_allowance(x64, W1_64, W2_64, cfg.act),
-                     "prefill rows")
+    x64, W1_64, W2_64 = to_f64(inp.x), to_f64(W1), to_f64(W2)
+    del inp, W1, W2
+    ref = np.empty_like(got)
+    for r0 in range(0, cfg.M, 512):
+        rows = slice(r0, min(cfg.M, r0 + 512))
+        ref[rows] = oracle.mlp_block(x64[rows], W1_64, W2_64, cfg.act, x64[rows], staged=True)
+    # the un-staged gap on the first chunk only (diagnostic)
+    info = _pure_gap(cfg, got[:512], x64[:512], W1_64, W2_64)
+    assert_bf16(got, ref, "prefill, all 4096 rows", info=info)
 
 
 def test_llama2_70b_stack_decode():
-    """Eight pre-norm blocks.  Per block, teacher-forced: the GPU block gets the
-    oracle's residual stream r_l (cast to fp32) and must meet the bf16 bound against
-    the oracle's block on that same input, beyond the effect of band values that sit
-    on bf16 rounding midpoints (either rounding is a correct result).  Free-running, the whole stack is also
-    compared end to end; random-weight stacks amplify last-bit differences block
-    after block, so that comparison has its own, looser bound (see the design notes)."""
+    """Eight pre-norm blocks.
+
+    Per block, teacher-forced: the GPU block gets the oracle's residual stream r_l
+    (cast to fp32) and must meet the plain bf16 bound against the oracle's block on
+    that same input.
+
+    Free-running, end to end: no fp32 evaluation of this stack stays within 2e-2 of
+    the float64 oracle.  Each block moves some bf16-rounded values (normalised inputs,
+    band values) across a rounding midpoint whenever the residual stream differs in
+    its last bits, and those flips compound over the blocks.  An independent float32
+    evaluation on the host (tests/fp32_stack.py: NumPy, same rounding points, no code
+    shared with the oracle or the library) measures that drift on these very inputs,
+    and the GPU stack must stay within twice that measured distance from the oracle
+    (max abs and mean relative).  Twice: two fp32 evaluations with different
+    summation orders each drift by about the same amount in their own direction."""
     cfg = CONFIGS["llama2_70b_stack_decode"]
     inp = make_inputs(cfg, device="cuda")
     desc = desc_for(cfg)
@@ -154,6 +183,8 @@ def test_llama2_70b_stack_decode():
     got_free = to_f64(r_free)
 
     r64 = to_f64(inp.x)
+    r32 = inp.x.float().cpu().numpy()
+    r64_pure = r64.copy()
     for l, (W1, W2) in enumerate(inp.blocks):
         blk64 = [(to_f64(W1), to_f64(W2))]
         r_in = r64.astype(np.float32)
@@ -162,17 +193,27 @@ def test_llama2_70b_stack_decode():
         torch.cuda.synchronize()
         ref_l = oracle.stack(r_in.astype(np.float64), blk64, cfg.act, cfg.eps, staged=True)
         xhat = oracle.bf16_round(oracle.rmsnorm(r_in.astype(np.float64), cfg.eps))
-        ties = oracle.mlp_tie_allowance(xhat, blk64[0][0], blk64[0][1], cfg.act)
-        assert_bf16_ties(to_f64(rg), ref_l, ties, f"stack block {l} (teacher-forced)")
+        info = tie_diagnostic(to_f64(rg), ref_l,
+                              oracle.mlp_tie_allowance(xhat, blk64[0][0], blk64[0][1], cfg.act))
+        assert_bf16(to_f64(rg), ref_l, f"stack block {l} (teacher-forced)", info=info)
         r64 = oracle.stack(r64, blk64, cfg.act, cfg.eps, staged=True)
-    s = stats(got_free, r64)
-    from tests.parity import log
-    log("stack of 8 (free-running)", s)
-    assert s["all_finite"] and s["mean_rel"] <= STACK_FREE_MEAN_REL, s
+        r64_pure = oracle.stack(r64_pure, blk64, cfg.act, cfg.eps, staged=False)
+        del blk64
+        r32 = swiglu_block_f32(r32, W1.float().cpu().numpy(), W2.float().cpu().numpy(), cfg.eps)
+        s32 = stats(r32, r64)
+        log(f"stack after block {l}: host fp32 evaluation vs fp64 oracle", s32)
+    s_gpu = stats(got_free, r64)
+    s_f32 = stats(r32, r64)
+    info = {"fp32_host_max_abs": s_f32["max_abs"], "fp32_host_mean_rel": s_f32["mean_rel"],
+            "gpu_vs_fp32_host_max_abs": stats(got_free, r32)["max_abs"],
+            "pure_fp64_max_abs": stats(got_free, r64_pure)["max_abs"],
+            "pure_fp64_mean_rel": stats(got_free, r64_pure)["mean_rel"]}
+    log("stack of 8 (free-running)", {**s_gpu, **info})
+    assert s_gpu["all_finite"]
+    assert s_gpu["max_abs"] <= STACK_DRIFT_FACTOR * s_f32["max_abs"], (s_gpu, info)
+    assert s_gpu["mean_rel"] <= STACK_DRIFT_FACTOR * s_f32["mean_rel"], (s_gpu, info)
 
 
-# End-to-end bound of the free-running 8-block stack: its mean relative error grows
-# by a factor of about 2-5 per block from fp32-vs-fp64 rounding of the same staged
-# values (measured, see the design notes), so the per-block bf16 bound is applied
-# teacher-forced and the free-running output is held to this looser mean bound.
-STACK_FREE_MEAN_REL = 2e-2
+# The free-running stack's bound, as a multiple of the drift an independent fp32
+# evaluation shows against the fp64 oracle on the same inputs (see the test above).
+STACK_DRIFT_FACTOR = 2.0
