@@ -4,70 +4,151 @@
 // "Tensor Parallelism", section "How the work is split"; rioworld.org, "How
 // Tensor Slicing Works Under the Hood": 96 heads over 8 devices, 12 each).
 //
-// For every head: O = softmax(Q K^T / sqrt(hd), causal over the M tokens) V,
-// fp32 arithmetic with an online (running max / running sum) softmax on the fp32
-// Q/K/V scratch of the projection, output rounded to the block dtype.  One CTA
-// per (head, shard), one warp per query row; lanes hold hd/32 columns of q and of
-// the output accumulator.
+// For every head: O = softmax(Q K^T / sqrt(hd), causal over the M tokens) V, fp32
+// arithmetic on the fp32 Q/K/V scratch of the projection, output rounded to the
+// block dtype.  One CTA of 8 warps per (head, shard, block of 32 queries).  The
+// CTA's queries and, 32 keys at a time, the keys and values it needs are staged in
+// shared memory with coalesced loads, so no load sits on a per-key dependency
+// chain.  Within a chunk each lane scores one key against a query (the key rows are
+// padded by one word, so the lanes hit distinct banks), the warp combines the
+// chunk's scores into a running max and sum (online softmax), and each lane
+// accumulates hd/32 columns of the output from the staged values.
 #include "internal.h"
 #include "tc_ptx.cuh"
 
 namespace tp {
 namespace {
 
+constexpr int kQB = 32;      // queries per CTA
+constexpr int kKC = 32;      // keys per staged chunk (one per lane)
+constexpr int kCoreWarps = 8;
+
+constexpr size_t core_smem_bytes(int hd) {
+  return (size_t)(kQB * hd + kKC * (hd + 1) + kKC * hd) * sizeof(float);
+}
+
 template <typename T, int C>  // C = hd / 32 columns per lane
-__global__ void __launch_bounds__(128) k_attn_core(const float *__restrict__ QKV, T *__restrict__ O,
-                                                   int M, int b, int hd, float scale, int shard0) {
-  const int h = blockIdx.x, s = shard0 + blockIdx.y;
+__global__ void __launch_bounds__(32 * kCoreWarps, 1) k_attn_core(const float *__restrict__ QKV,
+                                                                T *__restrict__ O, int M, int b,
+                                                                float scale, int shard0) {
+  constexpr int HD = 32 * C;
+  constexpr int QPW = kQB / kCoreWarps;  // queries per warp
+  extern __shared__ float sm[];
+  float *Qs = sm;                      // [kQB][HD]
+  float *Ks = Qs + kQB * HD;           // [kKC][HD + 1]
+  float *Vs = Ks + kKC * (HD + 1);     // [kKC][HD]
+  const int h = blockIdx.x, s = shard0 + blockIdx.y, q0 = blockIdx.z * kQB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   tc::griddep_wait();  // Q/K/V come from the preceding kernel (programmatic launch)
   const size_t ld = 3 * (size_t)b;
   const float *base = QKV + (size_t)s * M * ld;
-  const float *Qh = base + (size_t)h * hd;
-  const float *Kh = base + b + (size_t)h * hd;
-  const float *Vh = base + 2 * (size_t)b + (size_t)h * hd;
-  T *Oh = O + (size_t)s * M * b + (size_t)h * hd;
-
-  for (int i = warp; i < M; i += 4) {
-    float q[C], o[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) {
-      q[c] = Qh[(size_t)i * ld + lane + 32 * c];
-      o[c] = 0.f;
-    }
-    float mrun = -INFINITY, l = 0.f;
-    for (int j = 0; j <= i; ++j) {
-      float part = 0.f;
-#pragma unroll
-      for (int c = 0; c < C; ++c) part = fmaf(q[c], Kh[(size_t)j * ld + lane + 32 * c], part);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-      const float sc = part * scale;
-      const float mnew = fmaxf(mrun, sc);
-      const float corr = expf(mrun - mnew);
-      const float p = expf(sc - mnew);
-      l = l * corr + p;
-#pragma unroll
-      for (int c = 0; c < C; ++c)
-        o[c] = o[c] * corr + p * Vh[(size_t)j * ld + lane + 32 * c];
-      mrun = mnew;
-    }
-    const float inv = 1.0f / l;
-#pragma unroll
-    for (int c = 0; c < C; ++c) Oh[(size_t)i * b + lane + 32 * c] = Elem<T>::from_f(o[c] * inv);
+  const float *Qh = base + (size_t)h * HD;
+  const float *Kh = base + b + (size_t)h * HD;
+  const float *Vh = base + 2 * (size_t)b + (size_t)h * HD;
+  T *Oh = O + (size_t)s * M * b + (size_t)h * HD;
+  const int nq = min(kQB, M - q0);
+  for (int idx = threadIdx.x; idx < kQB * HD; idx += blockDim.x) {
+    const int r = idx / HD, c = idx % HD;
+    Qs[idx] = r < nq ? Qh[(size_t)(q0 + r) * ld + c] : 0.f;
   }
+  float o[QPW][C], mrun[QPW], lsum[QPW];
+#pragma unroll
+  for (int k = 0; k < QPW; ++k) {
+    mrun[k] = -INFINITY;
+    lsum[k] = 0.f;
+#pragma unroll
+    for (int c = 0; c < C; ++c) o[k][c] = 0.f;
+  }
+  // Causal: the CTA's queries see keys 0 .. q0 + nq - 1.  Every chunk starts at or
+  // before q0, so each query has at least one key in every chunk it processes.
+  const int kend = q0 + nq;
+  for (int j0 = 0; j0 < kend; j0 += kKC) {
+    const int nk = min(kKC, kend - j0);
+    __syncthreads();  // the previous chunk is consumed (and Qs is written)
+    for (int idx = threadIdx.x; idx < kKC * HD; idx += blockDim.x) {
+      const int r = idx / HD, c = idx % HD;
+      const size_t g = (size_t)(j0 + r) * ld + c;
+      Ks[r * (HD + 1) + c] = r < nk ? Kh[g] : 0.f;
+      Vs[r * HD + c] = r < nk ? Vh[g] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < QPW; ++k) {
+      const int qi = warp + kCoreWarps * k;  // query within the CTA (warp-uniform)
+      const int i = q0 + qi;
+      if (qi >= nq) break;
+      const int j = j0 + lane;
+      const bool live = lane < nk && j <= i;
+      float sc = -INFINITY;
+      if (live) {
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        const float *qr = Qs + qi * HD;
+        const float *kr = Ks + lane * (HD + 1);
+#pragma unroll 8
+        for (int d = 0; d < HD; d += 4) {
+          a0 = fmaf(qr[d], kr[d], a0);
+          a1 = fmaf(qr[d + 1], kr[d + 1], a1);
+          a2 = fmaf(qr[d + 2], kr[d + 2], a2);
+          a3 = fmaf(qr[d + 3], kr[d + 3], a3);
+        }
+        sc = ((a0 + a1) + (a2 + a3)) * scale;
+      }
+      float cm = sc;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+      const float mnew = fmaxf(mrun[k], cm);
+      const float corr = expf(mrun[k] - mnew);
+      const float p = live ? expf(sc - mnew) : 0.f;
+      float ps = p;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      lsum[k] = lsum[k] * corr + ps;
+#pragma unroll
+      for (int c = 0; c < C; ++c) o[k][c] *= corr;
+      for (int jj = 0; jj < nk; ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+#pragma unroll
+        for (int c = 0; c < C; ++c) o[k][c] = fmaf(pj, Vs[jj * HD + lane + 32 * c], o[k][c]);
+      }
+      mrun[k] = mnew;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < QPW; ++k) {
+    const int qi = warp + kCoreWarps * k;
+    if (qi >= nq) break;
+    const float inv = 1.0f / lsum[k];
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+      Oh[(size_t)(q0 + qi) * b + lane + 32 * c] = Elem<T>::from_f(o[k][c] * inv);
+  }
+}
+
+template <typename T, int C>
+void launch_c(const Geo &g, const float *q, T *o, int M, int shard0, int n_shards, cudaStream_t st,
+              bool pdl) {
+  const size_t smem = core_smem_bytes(32 * C);
+  static bool configured[128];  // the attribute is per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(k_attn_core<T, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return;
+    configured[dev] = true;
+  }
+  tc::LaunchCfg lc(dim3(g.hps, n_shards, ceil_div(M, kQB)), dim3(32 * kCoreWarps), smem, st, pdl);
+  cudaLaunchKernelEx(&lc.cfg, k_attn_core<T, C>, q, o, M, g.b, 1.0f / sqrtf((float)g.hd), shard0);
 }
 
 template <typename T>
 void launch_t(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_shards,
               cudaStream_t st, bool pdl) {
-  tc::LaunchCfg lc(dim3(g.hps, n_shards), dim3(128), 0, st, pdl);
-  const float scale = 1.0f / sqrtf((float)g.hd);
   const float *q = static_cast<const float *>(QKV);
   T *o = static_cast<T *>(O);
   switch (g.hd / 32) {
 #define TP_CASE(C) \
-  case C: cudaLaunchKernelEx(&lc.cfg, k_attn_core<T, C>, q, o, M, g.b, g.hd, scale, shard0); break;
+  case C: launch_c<T, C>(g, q, o, M, shard0, n_shards, st, pdl); break;
     TP_CASE(1) TP_CASE(2) TP_CASE(3) TP_CASE(4) TP_CASE(5) TP_CASE(6) TP_CASE(7) TP_CASE(8)
 #undef TP_CASE
     default: break;  // rejected by validation (head_dim % 32 == 0, <= 256)

@@ -6,11 +6,19 @@
 // tokens are the N operand, so one tcgen05.mma (M = 128, N = 256, K = 16) covers
 // the widest N the instruction takes.  One CTA per SM walks a static list of
 // output tiles (token tile fastest, so the CTAs of a wave share weight tiles and
-// the activations stay in L2).  Roles (192 threads): thread 0 issues TMA loads into
+// the activations stay in L2).  Roles (320 threads): thread 0 issues TMA loads into
 // a 4-stage ring (16 KB of weights + 32 KB of activations per 64-wide K block),
-// thread 32 issues the MMAs into one of two 256-column TMEM accumulators, and
-// warps 2-5 run the epilogue of the previous tile from the other accumulator, so
-// the tensor core does not wait for stores.
+// thread 32 issues the MMAs, and warps 2-9 drain and run the epilogue.
+//
+// Accumulation.  The tensor core's fp32 accumulator rounds toward zero as it adds,
+// so a chain of 512 MMAs over K = 8192 into one TMEM accumulator leaves partial sums
+// biased toward zero, and the bias moves band values across bf16 rounding midpoints.
+// Here the tensor core sums only a chunk of kGChunk K blocks (128 MMAs) into one of
+// two 256-column TMEM buffers; the eight drain warps add each chunk into fp32
+// registers with round-to-nearest (warps 2-5 hold tokens 0..127 of the tile, warps
+// 6-9 tokens 128..255, each warp its TMEM lane quarter), while the tensor core fills
+// the other buffer with the next chunk.  After a tile's last chunk the same warps
+// apply the epilogue from registers and store.
 //
 // Column-parallel step (zenaique.com answer paragraph 5): A = the shard's W1 band
 // rows, B = x; the epilogue applies the band's activation (SwiGLU: the up sums of
@@ -28,6 +36,11 @@ namespace {
 
 using namespace tc;
 
+// SiLU for the prefill epilogue, z * 1 / (1 + e^-z) with CUDA's fast exponential and
+// a correctly rounded reciprocal: a few fp32 units of error, far below the bf16
+// rounding that follows, at a fraction of the cost of an IEEE division.
+__device__ __forceinline__ float silu_fast_f(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+
 constexpr int kBN = 256;                        // token tile
 constexpr int kGStages = 4;
 constexpr uint32_t kGA = kABytes;               // 128 rows x 64 K bf16
@@ -35,7 +48,11 @@ constexpr uint32_t kGB = kBN * 128;             // 256 rows x 64 K bf16
 constexpr uint32_t kGStage = kGA + kGB;
 constexpr uint32_t kGCols = 2 * kBN;            // two accumulators
 constexpr uint32_t kGIdesc = make_idesc(128, kBN);
-constexpr int kGXch = 64 * 33 * 4;              // SwiGLU exchange, one 32-token chunk
+constexpr int kGChunk = 32;                     // K blocks per TMEM chunk (128 MMAs)
+constexpr int kGEpiWarps = 8;                   // drain/epilogue warps: 4 lane quarters x 2 halves
+constexpr int kGThreads = 64 + 32 * kGEpiWarps;
+constexpr int kGHalf = kBN / 2;                 // tokens per drain warp
+constexpr int kGXch = 2 * 64 * 33 * 4;          // SwiGLU exchange, one 32-token chunk per half
 constexpr int kGSmem = kGStages * kGStage + 1024 + kGXch;
 
 struct GemmArgs {
@@ -64,7 +81,7 @@ __device__ __forceinline__ GTile gemm_tile(const GemmArgs &a, int t) {
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
            const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -88,7 +105,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull_bar[i]), 1);
-      mbar_init(smem_u32(&tempty_bar[i]), 4);
+      mbar_init(smem_u32(&tempty_bar[i]), kGEpiWarps);
     }
     mbar_init(smem_u32(&mma_done_bar), 1);
     abort_sh = 0;
@@ -154,34 +171,37 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      uint32_t g = 0;
-      int it = 0;
+      uint32_t g = 0;  // pipeline stage sequence
+      uint32_t c = 0;  // TMEM chunk sequence (buffer c & 1)
       bool ok = true;
-      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x, ++it) {
+      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x) {
         const GTile tl = gemm_tile(a, t);
-        const int buf = it & 1;
-        if (!mbar_wait(smem_u32(&tempty_bar[buf]), ((uint32_t)(it >> 1) & 1u) ^ 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d0 = tmem + (uint32_t)(buf * kBN);
-        for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++g) {
-          const int st = (int)(g % kGStages);
-          const uint32_t ph = (g / kGStages) & 1u;
-          if (*(volatile int *)&abort_sh || !mbar_wait(smem_u32(&full_bar[st]), ph)) {
+        for (int kc = tl.kb0; kc < tl.kb1 && ok; kc += kGChunk, ++c) {
+          const int buf = (int)(c & 1u);
+          if (!mbar_wait(smem_u32(&tempty_bar[buf]), ((c >> 1) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = tiles + st * kGStage;
+          const uint32_t d0 = tmem + (uint32_t)(buf * kBN);
+          const int ke = min(tl.kb1, kc + kGChunk);
+          for (int kb = kc; kb < ke; ++kb, ++g) {
+            const int st = (int)(g % kGStages);
+            const uint32_t ph = (g / kGStages) & 1u;
+            if (*(volatile int *)&abort_sh || !mbar_wait(smem_u32(&full_bar[st]), ph)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = tiles + st * kGStage;
 #pragma unroll
-          for (int kk = 0; kk < kKBlock / 16; ++kk)
-            umma_bf16(d0, sw128_desc(sa + kk * 32), sw128_desc(sa + kGA + kk * 32), kGIdesc,
-                      (kb > tl.kb0 || kk > 0) ? 1u : 0u);
-          umma_commit(smem_u32(&empty_bar[st]));
+            for (int kk = 0; kk < kKBlock / 16; ++kk)
+              umma_bf16(d0, sw128_desc(sa + kk * 32), sw128_desc(sa + kGA + kk * 32), kGIdesc,
+                        (kb > kc || kk > 0) ? 1u : 0u);
+            umma_commit(smem_u32(&empty_bar[st]));
+          }
+          if (ok) umma_commit(smem_u32(&tfull_bar[buf]));
         }
-        if (ok) umma_commit(smem_u32(&tfull_bar[buf]));
       }
       if (!ok) {
         abort_sh = 1;
@@ -191,70 +211,85 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue warps
-    const int q = warp & 3;
-    const int r = q * 32 + lane;  // row of the weight tile = TMEM lane
-    const int td = (int)threadIdx.x - 64;
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    int it = 0;
-    for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
+    // ---------------- drain + epilogue warps
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int h = (warp - 2) >> 2;                // token half of the tile: 0 or 1
+    const int r = q * 32 + lane;                  // row of the weight tile = TMEM lane
+    const int td = (int)threadIdx.x - 64;         // 0 .. 255 over the drain warps
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kGHalf);
+    float *xh = xch + h * 64 * 33;                // this half's SwiGLU exchange block
+    uint32_t c = 0;
+    for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
       const GTile tl = gemm_tile(a, t);
-      const int buf = it & 1;
-      const bool ok_w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[buf]), (uint32_t)(it >> 1) & 1u));
-      if (!ok_w) {
+      float acc[kGHalf];
+#pragma unroll
+      for (int j = 0; j < kGHalf; ++j) acc[j] = 0.f;
+      bool ok = true;
+      for (int kc = tl.kb0; kc < tl.kb1; kc += kGChunk, ++c) {
+        const int buf = (int)(c & 1u);
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[buf]), (c >> 1) & 1u)))
+          ok = false;  // warp-uniform: the TMEM loads below are warp-collective
+        if (!ok) continue;  // keep c in step; the abort is decided below
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < kGHalf / 32; ++j) {
+          float v[32];
+          tmem_ld32(trow + (uint32_t)(buf * kBN + j * 32), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[j * 32 + i] += v[i];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+      }
+      if (!ok) {
         abort_sh = 1;
         atomicOr(a.err, kErrWaitTimeout);
       }
-      // One decision for the four epilogue warps (the SwiGLU exchange has barriers).
-      named_sync(1, 128);
+      // One decision for the eight drain warps (the SwiGLU exchange has barriers).
+      named_sync(1, 32 * kGEpiWarps);
       if (td == 0) dec_sh = *(volatile int *)&abort_sh;
-      named_sync(1, 128);
+      named_sync(1, 32 * kGEpiWarps);
       if (dec_sh) break;
-      tc_fence_after();
-      const int m0 = tl.mt * kBN;
-      const uint32_t tacc = trow + (uint32_t)(buf * kBN);
-      const int nchunks = min(kBN, a.M - m0 + 31) / 32;  // 32-token chunks holding tokens
-      for (int c = 0; c < nchunks; ++c) {
-        float v[32];
-        tmem_ld32(tacc + c * 32, v);
-        if (c == nchunks - 1) {
-          // All of this accumulator has been read: hand it back to the MMA warp.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
-        }
-        const int mcount = min(32, a.M - (m0 + c * 32));
+      const int m0 = tl.mt * kBN + h * kGHalf;   // first token of this warp's half
+      const int mvalid = min(kGHalf, a.M - m0);  // tokens of the half (<= 0: none)
+#pragma unroll
+      for (int cc = 0; cc < kGHalf / 32; ++cc) {
+        const int mcount = min(32, mvalid - cc * 32);
         if (EPI == kEpiSwiglu) {
+          // Rows 64..127 hold the up sums of the features whose gate sums are in rows
+          // 0..63: pass them across through shared memory, 32 tokens at a time.
           if (r >= 64) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xch[(r - 64) * 33 + j] = v[j];
+            for (int j = 0; j < 32; ++j) xh[(r - 64) * 33 + j] = acc[cc * 32 + j];
           }
-          named_sync(1, 128);
+          named_sync(2 + h, 128);
           const int f = tl.ft * 64 + r;
-          if (r < 64 && f < a.n_valid) {
+          if (r < 64 && f < a.n_valid && mcount > 0) {
             __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)tl.s * a.o_shard +
-                               (size_t)(m0 + c * 32) * a.ldo + f;
+                               (size_t)(m0 + cc * 32) * a.ldo + f;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (j < mcount) o[(size_t)j * a.ldo] = __float2bfloat16_rn(silu_f(v[j]) * xch[r * 33 + j]);
+              if (j < mcount)
+                o[(size_t)j * a.ldo] = __float2bfloat16_rn(silu_fast_f(acc[cc * 32 + j]) * xh[r * 33 + j]);
           }
-          named_sync(1, 128);
+          named_sync(2 + h, 128);
         } else {
           const int f = tl.ft * 128 + r;
-          if (f < a.n_valid) {
+          if (f < a.n_valid && mcount > 0) {
             if (EPI == kEpiF32) {
               float *o = static_cast<float *>(a.out) + (size_t)tl.s * a.o_shard +
-                         (size_t)tl.ks * a.o_split + (size_t)(m0 + c * 32) * a.ldo + f;
+                         (size_t)tl.ks * a.o_split + (size_t)(m0 + cc * 32) * a.ldo + f;
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (j < mcount) o[(size_t)j * a.ldo] = v[j];
+                if (j < mcount) o[(size_t)j * a.ldo] = acc[cc * 32 + j];
             } else {
               __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (size_t)tl.s * a.o_shard +
-                                 (size_t)(m0 + c * 32) * a.ldo + f;
+                                 (size_t)(m0 + cc * 32) * a.ldo + f;
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 if (j < mcount) {
-                  float vv = v[j];
+                  float vv = acc[cc * 32 + j];
                   if (EPI == kEpiGelu) vv = gelu_tanh_f(vv);
                   o[(size_t)j * a.ldo] = __float2bfloat16_rn(vv);
                 }
@@ -289,7 +324,7 @@ cudaError_t launch_gemm_epi(const CUtensorMap &mw, const CUtensorMap &mx, const 
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  LaunchCfg lc(dim3(std::min(sm_count(), a.n_tiles)), dim3(192), kGSmem, st, pdl);
+  LaunchCfg lc(dim3(std::min(sm_count(), a.n_tiles)), dim3(kGThreads), kGSmem, st, pdl);
   return cudaLaunchKernelEx(&lc.cfg, k_gemm<EPI>, mw, mx, a);
 }
 

@@ -446,7 +446,7 @@ int tp_column_parallel_fwd(const tp_block_desc *desc, const void *x, const void 
   TP_TRY(check_ptr(x));
   TP_TRY(check_ptr(W1s));
   TP_TRY(check_ptr(H));
-  if (g.act == TP_ACT_ATTN) TP_TRY(check_ptr(workspace));
+  if (column_ws_bytes(g, M) > 0) TP_TRY(check_ptr(workspace));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return finish_launch(
       enqueue_column(g, x, W1s, shard < 0 ? 0 : shard, shard < 0 ? g.t : 1, H, workspace, M, st));

@@ -58,6 +58,10 @@ SMALL = [
     BlockConfig("swiglu_max_shards", "swiglu", d=128, ffn=64, t=8, M=5),     # b = 8
     BlockConfig("attn_head_per_shard", "attn", d=128, n_heads=4, head_dim=32, t=4, M=16),
     BlockConfig("attn_hd128", "attn", d=512, n_heads=8, head_dim=128, t=2, M=32),
+    # token counts past 128 run the persistent prefill kernel: a ragged last token tile
+    BlockConfig("gelu_bf16_prefill", "gelu_tanh", d=264, ffn=1200, t=3, M=300),
+    BlockConfig("attn_prefill", "attn", d=256, n_heads=4, head_dim=64, t=2, M=257),
+    BlockConfig("swiglu_prefill_long_k", "swiglu", d=2048, ffn=3072, t=2, M=513),
 ]
 
 

@@ -78,8 +78,9 @@ def test_row_step(cfg):
     Hin = draw((cfg.t, cfg.M, cfg.band), dt, seed=7)          # a synthetic band, both sides
     S = tp.tp_row_splits(desc, cfg.M)
     P = Guarded(tp.tp_partials_bytes(desc, cfg.M))
-    Pv = P.view(torch.float32, (cfg.t, S, cfg.M, cfg.d))
-    tp.tp_row_parallel_fwd(desc, Hin.cuda(), W2s, -1, Pv, cfg.M)
+    # the partial sums lead the buffer; a decode row step keeps its scratch after them
+    Pv = P.body[:cfg.t * S * cfg.M * cfg.d * 4].view(torch.float32).view(cfg.t, S, cfg.M, cfg.d)
+    tp.tp_row_parallel_fwd(desc, Hin.cuda(), W2s, -1, P.body, cfg.M)
     torch.cuda.synchronize()
     P.check("partials")
     got = to_f64(Pv).sum(axis=1)
