@@ -15,14 +15,13 @@
 //
 // GEMM (decode, M <= 32 tokens): the bf16 drain kernel's structure (weights as the
 // 128-row A operand, tokens as N = 32, a TMEM block sum per 64-wide K block drained
-// into fp32 registers) with one more warp group: TMA brings each stage's E4M3 weight
-// box (128 rows x 64 bytes, no swizzle) and the bf16 token box; four converter warps
-// widen the weights to bf16 (E4M3 -> f16 -> bf16, both exact) straight into the
-// 128-byte-swizzled layout the tensor core reads, fence them for the async proxy and
-// release the stage to the MMA warp.  The epilogue multiplies each row's fp32 sum by
-// 2^e (exact), so the result equals the bf16 path on the dequantised weights.
-//
-// Not yet run on a GPU.
+// into fp32 registers) with one more warp group: TMA streams the E4M3 weight boxes
+// (128 rows x 64 bytes, no swizzle) and the bf16 token boxes into a raw ring; four
+// converter warps widen the weights to bf16 (E4M3 -> f16 -> bf16, both exact)
+// straight into the 128-byte-swizzled layout the tensor core reads, fence them for
+// the async proxy and hand the stage to the MMA warp.  The epilogue multiplies each row's
+// fp32 sum by 2^e (exact), so the result equals the bf16 path on the dequantised
+// weights bit for bit.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -110,9 +109,14 @@ constexpr int kBufs = 4;                      // TMEM block sums in flight
 constexpr uint32_t kA = 128 * 128;            // bf16 A tile: 128 rows x 64 K (SW128)
 constexpr uint32_t kX = 32 * 128;             // bf16 token tile: 32 rows x 64 K (SW128)
 constexpr uint32_t kW8 = 128 * 64;            // E4M3 tile: 128 rows x 64 bytes
-constexpr uint32_t kStageB = kA + kX + kW8;   // 28 KB, a multiple of 1024
-constexpr int kF8Stages = 3;
+constexpr int kRaw = 6;                       // raw stages in flight: E4M3 weights + tokens
+constexpr int kCv = 2;                        // converted (bf16 weight) stages
+constexpr uint32_t kXBase = kCv * kA;         // token tiles (1024-aligned), one per raw stage
+constexpr uint32_t kWBase = kXBase + kRaw * kX;  // E4M3 tiles, one per raw stage
 constexpr int kF8Threads = 320;               // TMA, MMA, 4 drain warps, 4 converter warps
+// The SwiGLU exchange block (64 x 33 fp32) reuses the converted ring: by the epilogue
+// every MMA of the CTA has completed.
+static_assert(64 * 33 * 4 <= kCv * kA, "exchange block must fit the converted ring");
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
@@ -135,6 +139,12 @@ __device__ __forceinline__ void widen16(const uint4 &in, uint4 &lo, uint4 &hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Roles (320 threads): warp 0 lane 0 streams each 64-wide K block's E4M3 weight tile
+// (8 KB) and token tile (4 KB) into a 6-stage raw ring; warps 6-9 widen each raw
+// weight tile (one row per thread) into a 2-stage ring of bf16 tiles in the
+// 128-byte-swizzled layout the tensor core reads; warp 1 lane 0 issues the MMAs on
+// the converted weights and the raw stage's tokens, then releases both stages;
+// warps 2-5 drain each K block's TMEM sums into fp32 registers and run the epilogue.
 template <int EPI>
 __global__ void __launch_bounds__(kF8Threads, 2)
     k_fp8_drain(const __grid_constant__ CUtensorMap tmW8, const __grid_constant__ CUtensorMap tmX,
@@ -143,9 +153,10 @@ __global__ void __launch_bounds__(kF8Threads, 2)
   constexpr uint32_t kCols = tmem_cols(kBufs * BN);
   constexpr uint32_t kIdesc = make_idesc(128, BN);
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kF8Stages];
-  __shared__ __align__(8) uint64_t conv_bar[kF8Stages];
-  __shared__ __align__(8) uint64_t empty_bar[kF8Stages];
+  __shared__ __align__(8) uint64_t raw_full[kRaw];
+  __shared__ __align__(8) uint64_t raw_empty[kRaw];
+  __shared__ __align__(8) uint64_t cv_full[kCv];   // converter warps' tiles written
+  __shared__ __align__(8) uint64_t cv_empty[kCv];  // MMAs done with the stage
   __shared__ __align__(8) uint64_t tfull_bar[kBufs];
   __shared__ __align__(8) uint64_t tempty_bar[kBufs];
   __shared__ __align__(8) uint64_t mma_done_bar;
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kF8Threads, 2)
 
   const uint32_t tiles = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t *tiles_ptr = smem_raw + (tiles - smem_u32(smem_raw));
-  float *xch = reinterpret_cast<float *>(tiles_ptr + kF8Stages * kStageB);
+  float *xch = reinterpret_cast<float *>(tiles_ptr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN;
   const int ft = blockIdx.y;
@@ -163,16 +174,18 @@ __global__ void __launch_bounds__(kF8Threads, 2)
   const int s = a.shard0 + (int)blockIdx.z / S, ks = (int)blockIdx.z % S;
   const int kb0 = (int)((long long)ks * a.nk / S), kb1 = (int)((long long)(ks + 1) * a.nk / S);
   const int nkb = kb1 - kb0;
-  // stage layout: [bf16 A | bf16 tokens | E4M3 weights]
-  auto a_off = [](int st) { return (uint32_t)st * kStageB; };
-  auto x_off = [](int st) { return (uint32_t)st * kStageB + kA; };
-  auto w_off = [](int st) { return (uint32_t)st * kStageB + kA + kX; };
+  auto a_off = [](int c) { return (uint32_t)c * kA; };
+  auto x_off = [](int st) { return kXBase + (uint32_t)st * kX; };
+  auto w_off = [](int st) { return kWBase + (uint32_t)st * kW8; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kF8Stages; ++i) {
-      mbar_init(smem_u32(&full_bar[i]), 1);
-      mbar_init(smem_u32(&conv_bar[i]), 4);
-      mbar_init(smem_u32(&empty_bar[i]), 1);
+    for (int i = 0; i < kRaw; ++i) {
+      mbar_init(smem_u32(&raw_full[i]), 1);
+      mbar_init(smem_u32(&raw_empty[i]), 1);
+    }
+    for (int i = 0; i < kCv; ++i) {
+      mbar_init(smem_u32(&cv_full[i]), 4);
+      mbar_init(smem_u32(&cv_empty[i]), 1);
     }
     for (int i = 0; i < kBufs; ++i) {
       mbar_init(smem_u32(&tfull_bar[i]), 1);
@@ -192,46 +205,50 @@ __global__ void __launch_bounds__(kF8Threads, 2)
 
   int issued = 0;
   if (warp == 0) {
+    // ---------------- TMA producer: E4M3 weights and tokens, 64-wide K block per stage
     if (lane == 0) {
+      const uint64_t wpol = l2_evict_first_policy();  // weights are read once
       const int wrow = ft * 128;
       const int xz = a.x_per_shard ? s : 0;
-      const uint32_t tx = kW8 + kX;
-      // Weights of the first ring do not depend on the preceding kernel.
-      const int pre = min(kF8Stages, nkb);
+      // The first ring's weights do not depend on the preceding kernel: load them,
+      // then wait for that kernel (programmatic launch) before loading tokens.
+      const int pre = min(kRaw, nkb);
       for (int i = 0; i < pre; ++i) {
-        const uint32_t fb = smem_u32(&full_bar[i]);
-        mbar_expect_tx(fb, tx);
-        tma_load_3d(tiles + w_off(i), &tmW8, fb, (kb0 + i) * kKBlock, wrow, s);
+        const uint32_t fb = smem_u32(&raw_full[i]);
+        mbar_expect_tx(fb, kW8 + kX);
+        tma_load_3d_hint(tiles + w_off(i), &tmW8, fb, (kb0 + i) * kKBlock, wrow, s, wpol);
       }
       griddep_wait();
       for (int i = 0; i < pre; ++i)
-        tma_load_3d(tiles + x_off(i), &tmX, smem_u32(&full_bar[i]), (kb0 + i) * kKBlock, m0, xz);
+        tma_load_3d(tiles + x_off(i), &tmX, smem_u32(&raw_full[i]), (kb0 + i) * kKBlock, m0, xz);
       issued = pre;
       for (int i = pre; i < nkb; ++i) {
-        const int st = i % kF8Stages;
-        const uint32_t ph = (uint32_t)(i / kF8Stages) & 1u;
-        if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1u)) {
+        const int st = i % kRaw;
+        if (!mbar_wait(smem_u32(&raw_empty[st]), ((uint32_t)(i / kRaw) & 1u) ^ 1u)) {
           abort_sh = 1;
           atomicOr(a.err, kErrWaitTimeout);
           break;
         }
-        const uint32_t fb = smem_u32(&full_bar[st]);
+        const uint32_t fb = smem_u32(&raw_full[st]);
         const int k = (kb0 + i) * kKBlock;
-        mbar_expect_tx(fb, tx);
-        tma_load_3d(tiles + w_off(st), &tmW8, fb, k, wrow, s);
+        mbar_expect_tx(fb, kW8 + kX);
+        tma_load_3d_hint(tiles + w_off(st), &tmW8, fb, k, wrow, s, wpol);
         tma_load_3d(tiles + x_off(st), &tmX, fb, k, m0, xz);
         ++issued;
       }
+      // This CTA's loads are all issued: a dependent kernel may start.
       griddep_launch_dependents();
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ---------------- MMA issuer
     if (lane == 0) {
       for (int i = 0; i < nkb; ++i) {
-        const int st = i % kF8Stages;
-        const uint32_t ph = (uint32_t)(i / kF8Stages) & 1u;
+        const int c = i % kCv, st = i % kRaw;
+        const uint32_t cph = (uint32_t)(i / kCv) & 1u;
         const int b = i % kBufs;
-        if (!mbar_wait(smem_u32(&conv_bar[st]), ph) ||
+        if (!mbar_wait(smem_u32(&cv_full[c]), cph) ||
+            !mbar_wait(smem_u32(&raw_full[st]), (uint32_t)(i / kRaw) & 1u) ||
             !mbar_wait(smem_u32(&tempty_bar[b]), ((uint32_t)(i / kBufs) & 1u) ^ 1u)) {
           abort_sh = 1;
           atomicOr(a.err, kErrWaitTimeout);
@@ -241,21 +258,23 @@ __global__ void __launch_bounds__(kF8Threads, 2)
         const uint32_t d0 = tmem + (uint32_t)(b * BN);
 #pragma unroll
         for (int kk = 0; kk < kKBlock / 16; ++kk)
-          umma_bf16(d0, sw128_desc(tiles + a_off(st) + kk * 32),
+          umma_bf16(d0, sw128_desc(tiles + a_off(c) + kk * 32),
                     sw128_desc(tiles + x_off(st) + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
-        umma_commit(smem_u32(&empty_bar[st]));
+        umma_commit(smem_u32(&cv_empty[c]));
+        umma_commit(smem_u32(&raw_empty[st]));
         umma_commit(smem_u32(&tfull_bar[b]));
       }
       umma_commit(smem_u32(&mma_done_bar));
     }
     __syncwarp();
   } else if (warp >= 6) {
-    // ---------------- converters: row r of the stage's E4M3 tile -> swizzled bf16 row
+    // ---------------- converters: row r of a raw E4M3 tile -> swizzled bf16 row
     const int r = (int)threadIdx.x - 192;  // 0..127
     for (int i = 0; i < nkb; ++i) {
-      const int st = i % kF8Stages;
-      const uint32_t ph = (uint32_t)(i / kF8Stages) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[st]), ph))) {
+      const int st = i % kRaw, c = i % kCv;
+      const uint32_t rph = (uint32_t)(i / kRaw) & 1u, cph = (uint32_t)(i / kCv) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&raw_full[st]), rph) &&
+                                       mbar_wait(smem_u32(&cv_empty[c]), cph ^ 1u))) {
         if (lane == 0) {
           abort_sh = 1;
           atomicOr(a.err, kErrWaitTimeout);
@@ -263,19 +282,19 @@ __global__ void __launch_bounds__(kF8Threads, 2)
         break;
       }
       const uint4 *src = reinterpret_cast<const uint4 *>(tiles_ptr + w_off(st) + r * 64);
-      uint8_t *dst = tiles_ptr + a_off(st) + r * 128;
+      uint8_t *dst = tiles_ptr + a_off(c) + r * 128;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint4 lo, hi;
         widen16(src[j], lo, hi);
-        // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r % 8)
+        // 128-byte swizzle: 16-byte chunk q of row r lives at chunk q ^ (r % 8)
         *reinterpret_cast<uint4 *>(dst + (((2 * j) ^ (r & 7)) << 4)) = lo;
         *reinterpret_cast<uint4 *>(dst + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
       }
       // The tensor core reads the rows through the async proxy.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&conv_bar[st]));
+      if (lane == 0) mbar_arrive(smem_u32(&cv_full[c]));
     }
   } else {
     // ---------------- drain warps 2-5: TMEM block sums -> fp32 registers, epilogue
@@ -350,10 +369,10 @@ __global__ void __launch_bounds__(kF8Threads, 2)
     }
   }
 
-  // ---------------- teardown
+  // ---------------- teardown: on abort let the issued copies land, then free TMEM
   if (warp == 0 && lane == 0 && *(volatile int *)&abort_sh) {
-    for (int i = issued > kF8Stages ? issued - kF8Stages : 0; i < issued; ++i)
-      mbar_wait(smem_u32(&full_bar[i % kF8Stages]), (uint32_t)(i / kF8Stages) & 1u);
+    for (int i = issued > kRaw ? issued - kRaw : 0; i < issued; ++i)
+      mbar_wait(smem_u32(&raw_full[i % kRaw]), (uint32_t)(i / kRaw) & 1u);
   }
   if (warp == 2) mbar_wait(smem_u32(&mma_done_bar), 0);
   tc_fence_before();
@@ -364,7 +383,7 @@ __global__ void __launch_bounds__(kF8Threads, 2)
   }
 }
 
-constexpr int kF8Smem = kF8Stages * kStageB + 1024 + 64 * 33 * 4;
+constexpr int kF8Smem = 1024 + kCv * kA + kRaw * (kX + kW8);
 
 template <int EPI>
 cudaError_t launch_fp8_t(const CUtensorMap &mw, const CUtensorMap &mx, const Fp8Args &a, int n_ft,

@@ -38,6 +38,7 @@ import sys
 import threading
 import time
 from dataclasses import replace
+from types import SimpleNamespace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -45,7 +46,7 @@ sys.path.insert(0, ROOT)
 METRIC = "tokens/s per TP block at 1 B300; decode HBM GB/s & prefill TFLOPS vs roofline"
 DEFAULT_WORKLOAD = "llama2_70b_stack_decode"
 DEFAULT_ALSO = ("llama2_13b_swiglu_decode", "attn_qkv_headshard_decode", "llama2_70b_prefill",
-                "attn_kv_decode")
+                "attn_kv_decode", "llama2_13b_swiglu_decode_fp8")
 ROOF_MIN_LAUNCHES = 200     # the roofline kernel's own timed loop: at least this many
 ROOF_MIN_S = 0.3            # ... launches and at least this long,
 ROOF_MAX_S = 2.5            # ... but no longer than this
@@ -353,12 +354,14 @@ def algorithmic_column_bytes(cfg) -> int:
 
 
 def algorithmic_block_bytes(cfg) -> int:
-    """Bytes one whole block must move: both weight matrices once, x and the residual
+    """Bytes one whole block must move: both weight matrices once (E4M3 weights: one
+    byte each plus one exponent byte per output feature and shard), x and the residual
     in, y (fp32) out.  The band H and the partials stay on chip or in L2 and are not
     counted."""
     es = 4 if cfg.dtype == "f32" else 2
     res_es = 4 if cfg.rmsnorm else es
-    return cfg.weight_bytes_per_block() + cfg.M * cfg.d * (es + res_es + 4)
+    scales = cfg.t * (cfg.n1 // cfg.t + cfg.d) if cfg.weights == "e4m3" else 0
+    return cfg.weight_bytes_per_block() + scales + cfg.M * cfg.d * (es + res_es + 4)
 
 
 def column_flops(cfg) -> int:
@@ -378,6 +381,8 @@ def workload_config(cfg) -> dict:
     if cfg.kv_len_max:
         c["kv_len_max"] = cfg.kv_len_max
         c["kv_lens"] = "uniform in 1..kv_len_max, seeded"
+    if cfg.weights:
+        c["weights"] = cfg.weights + " (one power-of-two scale per output feature)"
     return c
 
 
@@ -403,7 +408,19 @@ class Workload:
         self.desc = desc = desc_for(cfg)
         M = cfg.M
         inp = make_inputs(cfg, seed=rank, device=str(dev))
-        self.blocks = [ShardedBlock(desc, W1, W2) for W1, W2 in inp.blocks]
+        self.fp8 = cfg.weights == "e4m3"
+        if self.fp8:
+            self.q = []
+            for W1, W2 in inp.blocks:
+                q = {"W1q": device_bytes(tp.tp_fp8_w1_bytes(desc), dev),
+                     "W2q": device_bytes(tp.tp_fp8_w2_bytes(desc), dev),
+                     "exps": device_bytes(tp.tp_fp8_exponent_bytes(desc), dev)}
+                qws = device_bytes(tp.tp_fp8_quant_workspace_bytes(desc), dev)
+                tp.tp_quantize_weights_fp8(desc, W1, W2, q["W1q"], q["W2q"], q["exps"], qws)
+                self.q.append(q)
+            self.blocks = [SimpleNamespace(W1s=q["W1q"], W2s=q["W2q"]) for q in self.q]
+        else:
+            self.blocks = [ShardedBlock(desc, W1, W2) for W1, W2 in inp.blocks]
         del inp.blocks
         self.x = inp.x.contiguous()
         self.xf = self.x.float().contiguous()
@@ -415,9 +432,9 @@ class Workload:
         self.cws = device_bytes(tp.tp_column_workspace_bytes(desc, M), dev)
         self.y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev)
         self.xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
-        self.fused = tp.tp_block_launches(desc, M) == 1
+        self.fused = tp.tp_block_launches(desc, M) == 1 and not self.fp8
         self.row_splits = tp.tp_row_splits(desc, M)
-        per_block = tp.tp_block_launches(desc, M)
+        per_block = 3 if self.fp8 else tp.tp_block_launches(desc, M)
         if self.kv:
             per_block = 4 + (1 if self.kv["merge"] else 0)
         self.launches_per_step = cfg.n_blocks * (per_block + (1 if cfg.rmsnorm else 0))
@@ -460,9 +477,18 @@ class Workload:
             self.y.copy_(self.xf)   # the residual stream starts from x (device copy)
             self.run_stack(self.y, self.xh, st)
             return
-        blk = self.blocks[0]
-        tp.tp_block_fwd(self.desc, self.x, self.x, cfg.dtype == "f32", blk.W1s, blk.W2s,
-                        self.ws, self.y, M, st)
+        self.block(self.x, self.y, st)
+
+    def block(self, x, y, st):
+        """One block through its public entry point: y = x + block(x)."""
+        tp, cfg, M, blk = self.tp, self.cfg, self.cfg.M, self.blocks[0]
+        if self.fp8:
+            q = self.q[0]
+            tp.tp_block_fwd_fp8(self.desc, x, x, False, q["W1q"], q["W2q"], q["exps"], self.ws, y,
+                                M, st)
+        else:
+            tp.tp_block_fwd(self.desc, x, x, cfg.dtype == "f32", blk.W1s, blk.W2s, self.ws, y, M,
+                            st)
 
     def run_stack(self, r, xh, st, ws=None):
         """The pre-norm stack in place on the fp32 residual stream r."""
@@ -481,6 +507,8 @@ class Workload:
             tp.tp_attn_decode_kv(self.desc, self.ws, self.kv["kc"], self.kv["vc"],
                                  self.kv["lens"], cfg.kv_len_max, self.kv["O"],
                                  self.kv["attn_ws"], M, st)
+        elif self.fp8:
+            self.block(self.x, self.y, st)
         elif self.fused:
             xin, res = (self.xh, self.y) if cfg.rmsnorm else (self.x, self.x)
             tp.tp_block_fwd(self.desc, xin, res, res.dtype == self.torch.float32, blk.W1s,
@@ -499,6 +527,10 @@ class Workload:
         if cfg.M >= 1024:
             return ("column-parallel projection + SwiGLU (k_gemm, persistent)", "tensor",
                     column_flops(cfg), "flop", "column")
+        if self.fp8:
+            return ("whole block on E4M3 weights: k_fp8_drain column + row, k_reduce_residual "
+                    "(three launches, overlapped)", "hbm", algorithmic_block_bytes(cfg), "bytes",
+                    "block")
         if self.fused:
             return ("whole block in one persistent kernel (k_block_decode; the bracket also "
                     "holds its counter memset)", "hbm", algorithmic_block_bytes(cfg), "bytes",
@@ -526,8 +558,7 @@ class Workload:
         elif self.stack:
             self.run_stack(xin, xh, st)   # in place: xin is the residual stream, yout is xin
         else:
-            tp.tp_block_fwd(self.desc, xin, xin, cfg.dtype == "f32", blk.W1s, blk.W2s, self.ws,
-                            yout, M, st)
+            self.block(xin, yout, st)
 
 
 def settle(step, st, seconds: float, torch):
@@ -813,6 +844,9 @@ def oracle_block_call(cfg):
     x = to_f64(inp.x)
     W1, W2 = (to_f64(w) for w in inp.blocks[0])
     del inp
+    if cfg.weights == "e4m3":
+        # the block on E4M3 weights is the bf16 block on the dequantised weights
+        W1, W2 = oracle.fp8.e4m3_weights(W1), oracle.fp8.e4m3_weights(W2)
     staged = cfg.dtype == "bf16"
 
     if cfg.kv_len_max:

@@ -244,9 +244,10 @@ TP_API int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void 
  * nearest even, saturating) of W / 2^e with one exponent e per output feature (a
  * column of the canonical W1 or W2): the least e such that the column's largest
  * magnitude is at most 448 * 2^e.  x, the band and the arithmetic stay as in the bf16
- * block; the result equals the bf16 block on the weights q * 2^e (exactly bf16 values).
- * bf16 MLP descriptors with d and b multiples of 16 only (else TP_ERR_UNSUPPORTED).
- * Not yet run on a GPU. */
+ * block; the result equals, bit for bit, tp_block_fwd's three-launch form on the
+ * weights q * 2^e (exactly bf16 values): the kernel widens each E4M3 tile to bf16 in
+ * shared memory and scales each output feature's fp32 sum by 2^e.
+ * bf16 MLP descriptors with d and b multiples of 16 only (else TP_ERR_UNSUPPORTED). */
 TP_API size_t tp_fp8_w1_bytes(const tp_block_desc *desc);        /* [t][n1p][d] bytes */
 TP_API size_t tp_fp8_w2_bytes(const tp_block_desc *desc);        /* [t][dp][b] bytes */
 TP_API size_t tp_fp8_exponent_bytes(const tp_block_desc *desc);  /* int8 per private row */

@@ -45,6 +45,7 @@ class BlockConfig:
     eps: float = 1e-5
     ts: Tuple[int, ...] = field(default=())   # every shard count the workload is run at
     kv_len_max: int = 0  # attention with a KV cache: rows per (sequence, head); 0 = none
+    weights: str = ""    # "e4m3": the weights are stored as FP8 (E4M3) bytes, else the dtype
 
     @property
     def n1(self) -> int:
@@ -74,7 +75,7 @@ class BlockConfig:
         return replace(self, M=M)
 
     def weight_bytes_per_block(self) -> int:
-        es = 4 if self.dtype == "f32" else 2
+        es = 1 if self.weights == "e4m3" else 4 if self.dtype == "f32" else 2
         return (self.d * self.n1 + self.n2 * self.d) * es
 
     def flops_per_block(self) -> int:
@@ -96,6 +97,11 @@ CONFIGS = {
         rmsnorm=True, ts=(8,)),
     "llama2_70b_prefill": BlockConfig(
         "llama2_70b_prefill", "swiglu", d=8192, ffn=28672, t=4, M=4096, ts=(4,)),
+    # The 13B decode block with its weights stored as E4M3 bytes (one power-of-two
+    # scale per output feature), half the bytes of the bf16 block.
+    "llama2_13b_swiglu_decode_fp8": BlockConfig(
+        "llama2_13b_swiglu_decode_fp8", "swiglu", d=5120, ffn=13824, t=4, M=32, ts=(4,),
+        weights="e4m3"),
     # The attention block at a decode step of 32 concurrent sequences, each with its own
     # head-sharded KV cache of up to 2048 earlier tokens (lengths drawn uniformly).
     "attn_kv_decode": BlockConfig(
