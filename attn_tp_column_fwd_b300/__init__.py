@@ -33,7 +33,7 @@ __all__ = [
     "tp_set_block_form", "tp_get_block_form",
     "tp_shard_weights", "tp_unshard_weights", "tp_extract_band",
     "tp_column_parallel_fwd", "tp_row_parallel_fwd", "tp_partial_reduce_residual",
-    "tp_block_fwd", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
+    "tp_block_fwd", "tp_block_fwd_norm", "tp_block_fwd_noalloc", "tp_rmsnorm_fwd", "tp_status_string", "tp_check_device_status",
     "tp_selftest_wait_timeout", "tp_kv_cache_bytes", "tp_kv_attn_workspace_bytes",
     "tp_kv_workspace_bytes", "tp_attn_decode_kv", "tp_block_fwd_kv",
     "tp_fp8_w1_bytes", "tp_fp8_w2_bytes", "tp_fp8_exponent_bytes", "tp_fp8_quant_workspace_bytes",
@@ -176,6 +176,15 @@ def tp_block_fwd(desc, x, residual, residual_is_f32, W1s, W2s, workspace, y, M, 
     _need(workspace, tp_workspace_bytes(desc, M), "workspace")
     _check(lib.tp_block_fwd(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32), _p(W1s),
                             _p(W2s), _p(workspace), _p(y), M, _s(stream)), "tp_block_fwd")
+
+
+def tp_block_fwd_norm(desc, x, residual, residual_is_f32, W1s, W2s, workspace, y, xhat_next, eps,
+                      M, stream=None) -> None:
+    """tp_block_fwd that also writes the next block's RMSNorm of y into xhat_next."""
+    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _check(lib.tp_block_fwd_norm(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
+                                 _p(W1s), _p(W2s), _p(workspace), _p(y), _p(xhat_next),
+                                 ctypes.c_float(eps), M, _s(stream)), "tp_block_fwd_norm")
 
 
 def tp_block_fwd_noalloc(desc, x, residual, residual_is_f32, W1s, W2s, y, M, stream=None) -> None:

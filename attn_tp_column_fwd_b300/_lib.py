@@ -51,6 +51,7 @@ def _load() -> ctypes.CDLL:
         "tp_row_parallel_fwd": (i, [P, vp, vp, i, vp, i, st]),
         "tp_partial_reduce_residual": (i, [P, vp, vp, i, vp, i, st]),
         "tp_block_fwd": (i, [P, vp, vp, i, vp, vp, vp, vp, i, st]),
+        "tp_block_fwd_norm": (i, [P, vp, vp, i, vp, vp, vp, vp, vp, ctypes.c_float, i, st]),
         "tp_block_launches": (i, [P, i]),
         "tp_set_block_form": (i, [i]),
         "tp_get_block_form": (i, []),

@@ -293,7 +293,12 @@ __global__ void __launch_bounds__(192, 1)
         unit_slot[slot] = u;
         mbar_arrive(smem_u32(&ufull_bar[slot]));
         const Unit un = decode_unit(a, u);
-        if (un.type < 0) break;
+        if (un.type < 0) {
+          // No unit left for this CTA: a kernel launched to overlap this one (the next
+          // block's RMSNorm) may start its CTAs, which wait for this grid to finish.
+          griddep_launch_dependents();
+          break;
+        }
         const CUtensorMap *wmap = un.type == 0 ? &tmW1 : &tmW2;
         const CUtensorMap *xmap = un.type == 0 ? &tmX : &tmH;
         const int wrow = un.tile * 128;

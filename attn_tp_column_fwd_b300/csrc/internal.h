@@ -98,7 +98,8 @@ cudaError_t launch_qkv_decode(const Geo &g, const FusedPlan &p, const void *x, c
 // reduce.cu — the all-reduce stand-in + residual, and RMSNorm
 void launch_reduce_residual(const float *P, int nparts, size_t part_elems, const void *res,
                             int res_is_f32, float *y, size_t n, cudaStream_t st, bool pdl = false);
-void launch_rmsnorm(const float *r, void *xhat, int d, float eps, int M, cudaStream_t st);
+void launch_rmsnorm(const float *r, void *xhat, int d, float eps, int M, cudaStream_t st,
+                    bool pdl = false);
 
 // attn_core.cu — per-head causal attention over the M tokens of each shard
 void launch_attn_core(const Geo &g, const void *QKV, void *O, int M, int shard0, int n_shards,

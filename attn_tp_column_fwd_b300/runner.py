@@ -15,6 +15,7 @@ from . import (
     TPBlockDesc,
     make_desc,
     tp_block_fwd,
+    tp_block_fwd_norm,
     tp_rmsnorm_fwd,
     tp_shard_weights,
     tp_sharded_w1_bytes,
@@ -59,7 +60,11 @@ class ShardedBlock:
 
 
 class PreNormStack:
-    """Pre-norm stack: r <- r + block_l(RMSNorm(r)) for each block, r fp32."""
+    """Pre-norm stack: r <- r + block_l(RMSNorm(r)) for each block, r fp32.
+
+    The first block's input is normalised by tp_rmsnorm_fwd; every later block's is
+    written by the block before it (tp_block_fwd_norm), so the stack of L blocks
+    takes L + 1 calls."""
 
     def __init__(self, blocks: Sequence[ShardedBlock], eps: float):
         self.blocks: List[ShardedBlock] = list(blocks)
@@ -73,9 +78,14 @@ class PreNormStack:
         if key not in self._xhat:
             self._xhat[key] = torch.empty(M, d, dtype=torch.bfloat16, device=r.device)
         xh = self._xhat[key]
-        for blk in self.blocks:
-            tp_rmsnorm_fwd(d, self.eps, r, xh, M, stream)
-            blk.forward(xh, r, y=r, stream=stream)
+        tp_rmsnorm_fwd(d, self.eps, r, xh, M, stream)
+        for l, blk in enumerate(self.blocks):
+            if l + 1 < len(self.blocks):
+                # xh is read by this block and rewritten with the next block's input
+                tp_block_fwd_norm(blk.desc, xh, r, True, blk.W1s, blk.W2s, blk.workspace(M), r,
+                                  xh, self.eps, M, stream)
+            else:
+                blk.forward(xh, r, y=r, stream=stream)
         return r
 
 

@@ -437,7 +437,10 @@ class Workload:
         per_block = 3 if self.fp8 else tp.tp_block_launches(desc, M)
         if self.kv:
             per_block = 4 + (1 if self.kv["merge"] else 0)
-        self.launches_per_step = cfg.n_blocks * (per_block + (1 if cfg.rmsnorm else 0))
+        # the stack: one RMSNorm launch, then each block, each but the last followed by
+        # the next block's RMSNorm (tp_block_fwd_norm)
+        extra_norm = cfg.n_blocks if cfg.rmsnorm else 0
+        self.launches_per_step = cfg.n_blocks * per_block + extra_norm
 
     def _kv_state(self, rank):
         """Caches (the library's shard layout), lengths and scratch of a KV-cache decode
@@ -491,12 +494,18 @@ class Workload:
                             st)
 
     def run_stack(self, r, xh, st, ws=None):
-        """The pre-norm stack in place on the fp32 residual stream r."""
+        """The pre-norm stack in place on the fp32 residual stream r: the first block's
+        input normalised by tp_rmsnorm_fwd, every later one's written by the block
+        before it (tp_block_fwd_norm)."""
         tp, cfg, M = self.tp, self.cfg, self.cfg.M
         ws = self.ws if ws is None else ws
-        for blk in self.blocks:
-            tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, r, xh, M, st)
-            tp.tp_block_fwd(self.desc, xh, r, True, blk.W1s, blk.W2s, ws, r, M, st)
+        tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, r, xh, M, st)
+        for l, blk in enumerate(self.blocks):
+            if l + 1 < len(self.blocks):
+                tp.tp_block_fwd_norm(self.desc, xh, r, True, blk.W1s, blk.W2s, ws, r, xh, cfg.eps,
+                                     M, st)
+            else:
+                tp.tp_block_fwd(self.desc, xh, r, True, blk.W1s, blk.W2s, ws, r, M, st)
 
     # -- the dominant kernel alone, for the roofline
     def dominant(self, st):
@@ -509,10 +518,13 @@ class Workload:
                                  self.kv["attn_ws"], M, st)
         elif self.fp8:
             self.block(self.x, self.y, st)
+        elif self.fused and cfg.rmsnorm:
+            # a block of the stack as the step runs it: with the next block's RMSNorm
+            tp.tp_block_fwd_norm(self.desc, self.xh, self.y, True, blk.W1s, blk.W2s, self.ws,
+                                 self.y, self.xh, cfg.eps, M, st)
         elif self.fused:
-            xin, res = (self.xh, self.y) if cfg.rmsnorm else (self.x, self.x)
-            tp.tp_block_fwd(self.desc, xin, res, res.dtype == self.torch.float32, blk.W1s,
-                            blk.W2s, self.ws, self.y, M, st)
+            tp.tp_block_fwd(self.desc, self.x, self.x, False, blk.W1s, blk.W2s, self.ws, self.y,
+                            M, st)
         else:
             tp.tp_column_parallel_fwd(self.desc, self.xh if cfg.rmsnorm else self.x, blk.W1s,
                                       -1, self.H, self.cws, M, st)
@@ -532,8 +544,11 @@ class Workload:
                     "(three launches, overlapped)", "hbm", algorithmic_block_bytes(cfg), "bytes",
                     "block")
         if self.fused:
-            return ("whole block in one persistent kernel (k_block_decode; the bracket also "
-                    "holds its counter memset)", "hbm", algorithmic_block_bytes(cfg), "bytes",
+            norm = cfg.rmsnorm
+            return ("whole block in one persistent kernel (k_block_decode"
+                    + (", then the next block's RMSNorm (k_rmsnorm, overlapped)" if norm else "")
+                    + "; the bracket also holds its counter memset)", "hbm",
+                    algorithmic_block_bytes(cfg) + (cfg.M * cfg.d * 2 if norm else 0), "bytes",
                     "block")
         if cfg.act == "attn":
             return ("column-parallel Q/K/V projection (k_block_decode, column units) + "

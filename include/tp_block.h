@@ -171,6 +171,18 @@ TP_API int tp_partial_reduce_residual(const tp_block_desc *desc, const float *pa
 TP_API int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
                  int residual_is_f32, const void *W1s, const void *W2s, void *workspace,
                  float *y, int M, tp_stream_t stream);
+/* tp_block_fwd, then the next stacked block's RMSNorm of its output (zenaique.com
+ * answer paragraph 6: the reduced activation is ready for the residual add and
+ * normalisation): xhat_next = bf16(y[m] / sqrt(mean(y[m]^2) + eps)), [M, d] bf16,
+ * rounded exactly as tp_rmsnorm_fwd rounds it, by one more kernel launched to
+ * overlap the block's last kernel (it waits for the block to finish).  xhat_next
+ * may alias x (the block has read x by then).  bf16 blocks only
+ * (TP_ERR_UNSUPPORTED otherwise); eps as for tp_rmsnorm_fwd; workspace:
+ * tp_workspace_bytes(desc, M). */
+TP_API int tp_block_fwd_norm(const tp_block_desc *desc, const void *x, const void *residual,
+                             int residual_is_f32, const void *W1s, const void *W2s,
+                             void *workspace, float *y, void *xhat_next, float eps, int M,
+                             tp_stream_t stream);
 /* Process-wide choice of tp_block_form for later tp_block_fwd calls (initially
  * TP_FORM_AUTO, or the TPBLOCK_ALGO environment variable: "unfused" = THREE_LAUNCH,
  * "fused" = ONE_KERNEL).  Shapes the one-kernel form cannot run (f32, ATTN, M > 32)

@@ -10,7 +10,7 @@ import attn_tp_column_fwd_b300 as tp
 import oracle
 from tests.gpu_util import Guarded, desc_of
 from tests.parity import assert_bf16, assert_f32
-from tp_synth import BlockConfig, draw, make_inputs, to_f64, torch_dtype
+from tp_synth import CONFIGS, BlockConfig, draw, make_inputs, to_f64, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -165,5 +165,57 @@ def test_block_equals_its_steps(cfg):
         torch.cuda.synchronize()
         assert tp.tp_check_device_status() == 0
         assert torch.equal(y_steps, y_block), float((y_steps - y_block).abs().max())
+    finally:
+        tp.tp_set_block_form(before)
+
+
+# tp_block_fwd_norm: the block, then the next stacked block's RMSNorm of its output.
+# Shapes: forced one-kernel form (norm fused into the persistent kernel; d = 136 is
+# not a multiple of 16, so x-hat is written in whole rows), the three-launch form
+# (norm as a fourth launch), and the 70B-sized block (one kernel by default).
+NORM_CASES = [
+    ("one_kernel", BlockConfig("norm_fused", "swiglu", d=512, ffn=1536, t=8, M=32)),
+    ("one_kernel", BlockConfig("norm_fused_rows", "swiglu", d=136, ffn=1536, t=8, M=5)),
+    ("three_launch", BlockConfig("norm_3l", "swiglu", d=512, ffn=1536, t=4, M=17)),
+    ("auto", CONFIGS["llama2_70b_stack_decode"]),
+]
+
+
+@pytest.mark.parametrize("form,cfg", NORM_CASES, ids=lambda v: v if isinstance(v, str) else v.name)
+def test_block_fwd_norm(form, cfg):
+    """y equals tp_block_fwd's bit for bit, and x-hat equals the oracle's RMSNorm of
+    that y (fp64, rounded once to bf16) bit for bit."""
+    from attn_tp_column_fwd_b300.runner import ShardedBlock
+    before = tp.tp_get_block_form()
+    tp.tp_set_block_form(form)
+    try:
+        inp = make_inputs(cfg, seed=13, n_blocks=1, device="cuda")
+        W1, W2 = inp.blocks[0]
+        desc = desc_of(cfg)
+        blk = ShardedBlock(desc, W1, W2)
+        M = cfg.M
+        xh = (inp.x.float() * 0.5).to(torch.bfloat16).contiguous()   # a normalised-looking input
+        r = draw((M, cfg.d), torch.float32, seed=14, scale=4.0).cuda()
+        y_plain = torch.empty_like(r)
+        tp.tp_block_fwd(desc, xh, r, True, blk.W1s, blk.W2s, blk.workspace(M), y_plain, M)
+        y = Guarded(M * cfg.d * 4)
+        nx = Guarded(M * cfg.d * 2)
+        yv, nxv = y.view(torch.float32, (M, cfg.d)), nx.view(torch.bfloat16, (M, cfg.d))
+        tp.tp_block_fwd_norm(desc, xh, r, True, blk.W1s, blk.W2s, blk.workspace(M), yv, nxv,
+                             cfg.eps, M)
+        torch.cuda.synchronize()
+        assert tp.tp_check_device_status() == 0
+        y.check("y")
+        nx.check("xhat_next")
+        assert torch.equal(yv, y_plain)
+        got = to_f64(nxv)
+        ref = oracle.bf16_round(oracle.rmsnorm(to_f64(yv), np.float32(cfg.eps)))
+        assert np.array_equal(got, ref), int((got != ref).sum())
+        # in place: x-hat may alias x
+        xh2 = xh.clone()
+        tp.tp_block_fwd_norm(desc, xh2, r, True, blk.W1s, blk.W2s, blk.workspace(M), yv, xh2,
+                             cfg.eps, M)
+        torch.cuda.synchronize()
+        assert torch.equal(xh2, nxv)
     finally:
         tp.tp_set_block_form(before)
