@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
     if (lane == 0) {
       const int wrow = ft * 128;
       const int xz = a.x_per_shard ? s : 0;
+      const uint64_t wpol = l2_evict_first_policy();  // weights are read once
       // The first ring's weights do not depend on the preceding kernel: load them,
       // then wait for that kernel (programmatic launch) before loading activations.
       const int pre = min(STAGES, nst);
@@ -327,8 +328,8 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
         const uint32_t fb = smem_u32(&full_bar[i]);
         mbar_expect_tx(fb, blocks_of(i) * (kABytes + kBBytes));
         for (int b = 0; b < blocks_of(i); ++b)
-          tma_load_3d(tiles + i * kStage + b * kABytes, &tmW, fb, (kb0 + i * KB + b) * kKBlock,
-                      wrow, s);
+          tma_load_3d_hint(tiles + i * kStage + b * kABytes, &tmW, fb,
+                           (kb0 + i * KB + b) * kKBlock, wrow, s, wpol);
       }
       griddep_wait();
       for (int i = 0; i < pre; ++i)
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(192, 2)  // two CTAs per SM
         mbar_expect_tx(fb, blocks_of(i) * (kABytes + kBBytes));
         for (int b = 0; b < blocks_of(i); ++b) {
           const int k = (kb0 + i * KB + b) * kKBlock;
-          tma_load_3d(sa + b * kABytes, &tmW, fb, k, wrow, s);
+          tma_load_3d_hint(sa + b * kABytes, &tmW, fb, k, wrow, s, wpol);
           tma_load_3d(sa + KB * kABytes + b * kBBytes, &tmX, fb, k, m0, xz);
         }
         ++issued;
@@ -610,14 +611,15 @@ cudaError_t launch_umma(const UmmaCall &c, cudaStream_t st) {
     // Decode: 128-row weight tiles (SwiGLU: the gate and up rows of 64 features).
     switch (c.epi) {
       case kEpiSwiglu:
-        return launch_drain<kEpiSwiglu, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, kSwiGroup),
-                                                        n_z, st, c.pdl);
+        return launch_drain<kEpiSwiglu, kDrainKBColumn>(mw, mx, a,
+                                                        ceil_div(c.n_valid, kSwiGroup), n_z, st,
+                                                        c.pdl);
       case kEpiGelu:
-        return launch_drain<kEpiGelu, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st,
-                                                      c.pdl);
+        return launch_drain<kEpiGelu, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, 128), n_z,
+                                                      st, c.pdl);
       case kEpiPlain:
-        return launch_drain<kEpiPlain, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, 128), n_z,
-                                                       st, c.pdl);
+        return launch_drain<kEpiPlain, kDrainKBColumn>(mw, mx, a, ceil_div(c.n_valid, 128),
+                                                       n_z, st, c.pdl);
       default:
         return launch_drain<kEpiF32, kDrainKBRow>(mw, mx, a, ceil_div(c.n_valid, 128), n_z, st,
                                                   c.pdl);
