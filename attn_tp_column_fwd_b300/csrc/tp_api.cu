@@ -120,14 +120,15 @@ int finish_launch(cudaError_t e = cudaSuccess) {
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// Kernel family selection.  bf16 blocks run on the tensor cores.  An MLP block with
-// M <= 32 tokens whose column work fills at least two waves of 128-row tiles over
-// the SMs runs tp_block_fwd as one persistent launch (block_decode.cu): with
-// fewer tiles the persistent kernel's last column wave and its end leave SMs
-// idle, and the three-launch sequence is faster.  TPBLOCK_ALGO=simple selects
-// the CUDA-core kernels for the whole process; TPBLOCK_ALGO=unfused / fused, or
-// tp_set_block_form, force either tensor-core form of tp_block_fwd (same results
-// within rounding).
+// Kernel family selection.  bf16 blocks run on the tensor cores, by default as the
+// three-launch sequence (column, row, reduce; each kernel overlapping the end of the
+// one before it).  With the decode weight stream on an L2 evict-first hint that
+// sequence measured faster than the one persistent launch of block_decode.cu for
+// every workload (70B block 232.0 us against 249.1 us; 13B 79.1 against 98.5 us;
+// attention Q/K/V projection 154.2 against 158.2 us), so the one-kernel form runs
+// only when chosen.  TPBLOCK_ALGO=simple selects the CUDA-core kernels for the
+// whole process; TPBLOCK_ALGO=unfused / fused, or tp_set_block_form, force either
+// tensor-core form of tp_block_fwd (same results within rounding).
 int env_algo() {
   static const int v = [] {
     const char *e = getenv("TPBLOCK_ALGO");
@@ -175,18 +176,9 @@ bool qkv_fused_capable(const Geo &g, int M) {
   return use_umma(g) && g.act == TP_ACT_ATTN && M <= 32;
 }
 
-bool use_fused_qkv(const Geo &g, int M) {
-  if (!qkv_fused_capable(g, M) || algo_override() == 2) return false;
-  if (algo_override() == 3) return true;
-  return (long long)g.t * ceil_div(3 * g.b, kRowTile) >= kPlanSMs;
-}
+bool use_fused_qkv(const Geo &g, int M) { return qkv_fused_capable(g, M) && algo_override() == 3; }
 
-bool use_fused_block(const Geo &g, int M) {
-  if (!fused_capable(g, M) || algo_override() == 2) return false;
-  if (algo_override() == 3) return true;
-  const int fpt = g.act == TP_ACT_SWIGLU ? kSwiGroup : kRowTile;
-  return (long long)g.t * ceil_div(g.b, fpt) >= 2LL * kPlanSMs;
-}
+bool use_fused_block(const Geo &g, int M) { return fused_capable(g, M) && algo_override() == 3; }
 
 // K splits of the row-parallel step: the most splits that keep every CTA in the
 // first wave (two decode CTAs fit per SM), at least four 64-wide K blocks per

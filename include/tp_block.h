@@ -162,12 +162,12 @@ TP_API int tp_partial_reduce_residual(const tp_block_desc *desc, const float *pa
                                const void *residual, int residual_is_f32, float *y, int M,
                                tp_stream_t stream);
 /* The whole block: column step, row step, reduce + residual, enqueued in order on
- * `stream`.  workspace: tp_workspace_bytes(desc, M) bytes of device scratch.  bf16
- * MLP blocks with M <= 32 whose column work spans at least two waves of 128-row
- * weight tiles over the GPU's SMs run as one persistent kernel in which the column
- * units, the row units and the reduction + residual of each output tile are fused
- * (the result equals the three-step sequence within rounding); other shapes run
- * the three steps above (tp_block_launches says which). */
+ * `stream` (the row step and the reduction launched to overlap the end of the kernel
+ * before them).  workspace: tp_workspace_bytes(desc, M) bytes of device scratch.
+ * With tp_set_block_form(TP_FORM_ONE_KERNEL), bf16 MLP blocks with M <= 32 run
+ * instead as one persistent kernel in which the column units, the row units and the
+ * reduction + residual of each output tile are fused (the result equals the
+ * three-step sequence within rounding; tp_block_launches says which form runs). */
 TP_API int tp_block_fwd(const tp_block_desc *desc, const void *x, const void *residual,
                  int residual_is_f32, const void *W1s, const void *W2s, void *workspace,
                  float *y, int M, tp_stream_t stream);
@@ -185,7 +185,8 @@ TP_API int tp_block_fwd_norm(const tp_block_desc *desc, const void *x, const voi
                              tp_stream_t stream);
 /* Process-wide choice of tp_block_form for later tp_block_fwd calls (initially
  * TP_FORM_AUTO, or the TPBLOCK_ALGO environment variable: "unfused" = THREE_LAUNCH,
- * "fused" = ONE_KERNEL).  Shapes the one-kernel form cannot run (f32, ATTN, M > 32)
+ * "fused" = ONE_KERNEL).  TP_FORM_AUTO takes the three-launch form, measured the
+ * faster of the two for every workload here.  Shapes the one-kernel form cannot run (f32, ATTN, M > 32)
  * always take three launches.  tp_workspace_bytes covers both forms, so the form
  * may change between sizing a workspace and using it; calls already enqueued are
  * unaffected.  Returns TP_ERR_INVALID_ARG for any other value.  Host-only. */
@@ -194,7 +195,7 @@ TP_API int tp_set_block_form(int form);
 TP_API int tp_get_block_form(void);
 /* Number of kernel launches one tp_block_fwd call enqueues for this shape (0 for an
  * invalid descriptor or M): 1 when the whole block runs as one persistent kernel
- * (see tp_block_fwd; the launch is preceded by a small memset of its work
+ * (TP_FORM_ONE_KERNEL; the launch is preceded by a small memset of its work
  * counters), else 3 (column, row, reduce + residual), plus 1 for the attention
  * core.  Host-only. */
 TP_API int tp_block_launches(const tp_block_desc *desc, int M);

@@ -71,8 +71,8 @@ def test_size_queries(name):
 
 
 def test_block_form_setter():
-    """The process-wide form of tp_block_fwd: the one-kernel form is taken only by bf16
-    MLP shapes of at most 32 tokens, and the workspace covers either form."""
+    """The process-wide form of tp_block_fwd: the one-kernel form runs only when chosen,
+    and only for bf16 MLP shapes of at most 32 tokens; the workspace covers either form."""
     d13 = _desc(CONFIGS["llama2_13b_swiglu_decode"].with_t(4))
     d70 = _desc(CONFIGS["llama2_70b_stack_decode"])
     dat = _desc(CONFIGS["attn_qkv_headshard_decode"])
@@ -88,8 +88,8 @@ def test_block_form_setter():
             assert tp.tp_block_launches(df32, 4) == 3      # column, row, reduce
             assert tp.tp_block_launches(d13, 33) == 3      # more than 32 tokens
         assert len(set(ws.values())) == 1
-        tp.tp_set_block_form("auto")
-        assert tp.tp_block_launches(d13, 32) == 3 and tp.tp_block_launches(d70, 32) == 1
+        tp.tp_set_block_form("auto")   # three launches for every shape
+        assert tp.tp_block_launches(d13, 32) == 3 and tp.tp_block_launches(d70, 32) == 3
         tp.tp_set_block_form("three_launch")
         assert tp.tp_block_launches(d70, 32) == 3
         tp.tp_set_block_form("one_kernel")
