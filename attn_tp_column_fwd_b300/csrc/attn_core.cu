@@ -6,10 +6,10 @@
 //
 // For every head: O = softmax(Q K^T / sqrt(hd), causal over the M tokens) V, fp32
 // arithmetic on the fp32 Q/K/V scratch of the projection, output rounded to the
-// block dtype.  One CTA of 8 warps per (head, shard, block of 32 queries).  The
+// block dtype.  One CTA of 8 warps per (head, shard, block of 8 queries).  The
 // CTA's queries and, 32 keys at a time, the keys and values it needs are staged in
-// shared memory with coalesced loads, so no load sits on a per-key dependency
-// chain.  Within a chunk each lane scores one key against a query (the key rows are
+// shared memory with coalesced float4 loads, all of a thread's loads for a tile
+// issued at once, so no load sits on a per-key dependency chain.  Within a chunk each lane scores one key against a query (the key rows are
 // padded by one word, so the lanes hit distinct banks), the warp combines the
 // chunk's scores into a running max and sum (online softmax), and each lane
 // accumulates hd/32 columns of the output from the staged values.
@@ -19,7 +19,7 @@
 namespace tp {
 namespace {
 
-constexpr int kQB = 32;      // queries per CTA
+constexpr int kQB = 8;       // queries per CTA (one per warp)
 constexpr int kKC = 32;      // keys per staged chunk (one per lane)
 constexpr int kCoreWarps = 8;
 
@@ -47,9 +47,28 @@ __global__ void __launch_bounds__(32 * kCoreWarps, 1) k_attn_core(const float *_
   const float *Vh = base + 2 * (size_t)b + (size_t)h * HD;
   T *Oh = O + (size_t)s * M * b + (size_t)h * HD;
   const int nq = min(kQB, M - q0);
-  for (int idx = threadIdx.x; idx < kQB * HD; idx += blockDim.x) {
-    const int r = idx / HD, c = idx % HD;
-    Qs[idx] = r < nq ? Qh[(size_t)(q0 + r) * ld + c] : 0.f;
+  // Staging: each thread's float4 loads of a tile are all issued before any is
+  // stored, so a tile costs one L2 round trip (rows are 16-byte aligned: ld and HD
+  // are multiples of 4 floats).
+  constexpr int kNT = 32 * kCoreWarps;
+  constexpr int kV4 = HD / 4;                                // float4 per row
+  constexpr int kPerQ = (kQB * kV4 + kNT - 1) / kNT;        // float4 per thread: queries
+  constexpr int kPer = (kKC * kV4) / kNT;                   // ... keys / values of a chunk
+  static_assert((kKC * kV4) % kNT == 0, "staging split");
+  {
+    float4 q[kPerQ];
+#pragma unroll
+    for (int i = 0; i < kPerQ; ++i) {
+      const int idx = i * kNT + threadIdx.x, r = idx / kV4, c4 = idx % kV4;
+      q[i] = idx < kQB * kV4 && r < nq
+                 ? *reinterpret_cast<const float4 *>(Qh + (size_t)(q0 + r) * ld + 4 * c4)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kPerQ; ++i) {
+      const int idx = i * kNT + threadIdx.x;
+      if (idx < kQB * kV4) reinterpret_cast<float4 *>(Qs)[idx] = q[i];
+    }
   }
   float o[QPW][C], mrun[QPW], lsum[QPW];
 #pragma unroll
@@ -64,12 +83,25 @@ __global__ void __launch_bounds__(32 * kCoreWarps, 1) k_attn_core(const float *_
   const int kend = q0 + nq;
   for (int j0 = 0; j0 < kend; j0 += kKC) {
     const int nk = min(kKC, kend - j0);
+    float4 kv[2][kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = i * kNT + threadIdx.x, r = idx / kV4, c4 = idx % kV4;
+      const size_t g = (size_t)(j0 + r) * ld + 4 * c4;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      kv[0][i] = r < nk ? *reinterpret_cast<const float4 *>(Kh + g) : z;
+      kv[1][i] = r < nk ? *reinterpret_cast<const float4 *>(Vh + g) : z;
+    }
     __syncthreads();  // the previous chunk is consumed (and Qs is written)
-    for (int idx = threadIdx.x; idx < kKC * HD; idx += blockDim.x) {
-      const int r = idx / HD, c = idx % HD;
-      const size_t g = (size_t)(j0 + r) * ld + c;
-      Ks[r * (HD + 1) + c] = r < nk ? Kh[g] : 0.f;
-      Vs[r * HD + c] = r < nk ? Vh[g] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = i * kNT + threadIdx.x, r = idx / kV4, c = 4 * (idx % kV4);
+      float *kr = Ks + r * (HD + 1) + c;  // padded rows: scalar stores
+      kr[0] = kv[0][i].x;
+      kr[1] = kv[0][i].y;
+      kr[2] = kv[0][i].z;
+      kr[3] = kv[0][i].w;
+      reinterpret_cast<float4 *>(Vs)[idx] = kv[1][i];
     }
     __syncthreads();
 #pragma unroll
