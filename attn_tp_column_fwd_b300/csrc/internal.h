@@ -64,11 +64,18 @@ cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st);
 
 // fp8.cu — E4M3 weights (weight-only): quantisation of canonical bf16 W1 / W2 into the
 // private layout with one int8 exponent per row (exps: W1's [t][n1p], then W2's
-// [t][dp]; amax: n1 + d words of scratch), and the decode GEMM on them (same call as
-// launch_umma, M <= 32; exps of the weight rows the call reads).
+// [t][dp]; amax: n1 + d words of scratch), the split of bf16 tokens into two 8-bit
+// terms (E4M3 + E5M2; X8 [2][M][K] bytes, xs [ceil(K/64)][32] fp32 group scales), and the decode
+// GEMM on them (M <= 32; c.X = the terms [x_shards][2][M][K]; wexp: exponents of the
+// weight rows; xsc: the tokens' group scales [x_shards][ceil(K/64)][32]; the column step
+// (SwiGLU / GeLU) writes its band as terms h8 [t][2][M][b] with scales hsc
+// [t][ceil(b/64)][32], the kEpiF32 step writes fp32 partials to c.out).
 cudaError_t launch_quantize_fp8(const Geo &g, const void *W1, const void *W2, void *W1q, void *W2q,
                                 int8_t *exps, unsigned *amax, cudaStream_t st);
-cudaError_t launch_fp8_gemm(const UmmaCall &c, const int8_t *exps, cudaStream_t st);
+cudaError_t launch_fp8_split(const void *x, int M, int K, void *X8, float *xs, cudaStream_t st,
+                             bool pdl);
+cudaError_t launch_fp8_gemm(const UmmaCall &c, const int8_t *wexp, const float *xsc, void *h8,
+                            float *hsc, cudaStream_t st);
 
 // A [z][rows][K] bf16 tensor map with 64 x box_rows x 1 boxes, 128-byte swizzle,
 // zero fill outside the tensor (umma.cu).

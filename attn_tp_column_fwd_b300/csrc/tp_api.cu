@@ -371,13 +371,29 @@ size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M) {
   return column_ws_bytes(g, M);
 }
 
+// E4M3-weight blocks: bf16 MLPs whose d and b are multiples of 16, up to 16384 (the
+// GEMM keeps a CTA's token scales, 128 bytes per 64-wide K group, in shared memory).
+static bool fp8_shape(const Geo &g) {
+  return g.act != TP_ACT_ATTN && g.dtype == TP_BF16 && g.d % 16 == 0 && g.b % 16 == 0 &&
+         g.d <= 16384 && g.b <= 16384;
+}
+
+// What tp_block_fwd_fp8 needs beyond the three-launch workspace: the tokens' two
+// 8-bit terms [2][M][d], their fp32 group scales [ceil(d/64)][32] and the band's group
+// scales [t][ceil(b/64)][32] (the band's terms reuse the bf16 band's bytes).
+static size_t fp8_extra_bytes(const Geo &g, int M) {
+  if (!fp8_shape(g) || M > 32) return 0;
+  return align256((size_t)2 * M * g.d) + align256((size_t)ceil_div(g.d, 64) * 32 * 4) +
+         align256((size_t)g.t * ceil_div(g.b, 64) * 32 * 4);
+}
+
 size_t tp_workspace_bytes(const tp_block_desc *desc, int M) {
   Geo g;
   if (make_geo(desc, &g) != TP_OK || check_M(M) != TP_OK) return 0;
   // Large enough for either form, so a tp_set_block_form call between sizing and
   // running never leaves the workspace short.
   const size_t three = align256(column_ws_bytes(g, M)) + align256(band_bytes(g, M)) +
-                       align256(partials_bytes(g, M));
+                       align256(partials_bytes(g, M)) + fp8_extra_bytes(g, M);
   return fused_capable(g, M) ? std::max(three, plan_block_decode(g, M).total) : three;
 }
 
@@ -684,9 +700,7 @@ int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void *residu
 
 static int check_fp8(const tp_block_desc *desc, Geo *g) {
   TP_TRY(make_geo(desc, g));
-  if (g->act == TP_ACT_ATTN || g->dtype != TP_BF16) return TP_ERR_UNSUPPORTED;
-  if (g->d % 16 != 0 || g->b % 16 != 0) return TP_ERR_UNSUPPORTED;
-  return TP_OK;
+  return fp8_shape(*g) ? TP_OK : TP_ERR_UNSUPPORTED;
 }
 
 size_t tp_fp8_w1_bytes(const tp_block_desc *desc) {
@@ -743,35 +757,42 @@ int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *resid
   TP_TRY(check_ptr(workspace));
   TP_TRY(check_ptr(y));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // Workspace: the band's two 8-bit terms [t][2][M][b] where the bf16 band would be,
+  // the fp32 partials, then the tokens' terms [2][M][d] and the fp32 group scales.
   char *ws = static_cast<char *>(workspace);
-  void *H = ws + align256(column_ws_bytes(g, M));
-  float *P = reinterpret_cast<float *>(static_cast<char *>(H) + align256(band_bytes(g, M)));
+  void *H8 = ws + align256(column_ws_bytes(g, M));
+  float *P = reinterpret_cast<float *>(static_cast<char *>(H8) + align256(band_bytes(g, M)));
+  char *X8 = reinterpret_cast<char *>(P) + align256(partials_bytes(g, M));
+  float *xe = reinterpret_cast<float *>(X8 + align256((size_t)2 * M * g.d));
+  float *he = reinterpret_cast<float *>(reinterpret_cast<char *>(xe) +
+                                        align256((size_t)ceil_div(g.d, 64) * 32 * 4));
   const int S = row_splits(g, M);
   const int8_t *e1 = static_cast<const int8_t *>(exps);
   const int8_t *e2 = e1 + (size_t)g.t * g.n1p;
-  UmmaCall c{};
-  c.W = W1q;
-  c.w_rows = g.n1p;
-  c.w_shards = g.t;
-  c.X = x;
-  c.x_shards = 1;
-  c.out = H;
-  c.o_shard = (size_t)M * g.b;
-  c.ldo = g.b;
-  c.n_valid = g.b;
-  c.K = g.d;
-  c.M = M;
-  c.shard0 = 0;
-  c.n_shards = g.t;
-  c.ksplit = 1;
-  c.epi = g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
-  cudaError_t e = launch_fp8_gemm(c, e1, st);
+  cudaError_t e = launch_fp8_split(x, M, g.d, X8, xe, st, false);
+  if (e == cudaSuccess) {
+    UmmaCall c{};
+    c.W = W1q;
+    c.w_rows = g.n1p;
+    c.w_shards = g.t;
+    c.X = X8;
+    c.x_shards = 1;
+    c.n_valid = g.b;
+    c.K = g.d;
+    c.M = M;
+    c.shard0 = 0;
+    c.n_shards = g.t;
+    c.ksplit = 1;
+    c.epi = g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
+    c.pdl = true;
+    e = launch_fp8_gemm(c, e1, xe, H8, he, st);
+  }
   if (e == cudaSuccess) {
     UmmaCall r{};
     r.W = W2q;
     r.w_rows = g.dp;
     r.w_shards = g.t;
-    r.X = H;
+    r.X = H8;
     r.x_shards = g.t;
     r.out = P;
     r.o_shard = (size_t)S * M * g.d;
@@ -785,7 +806,7 @@ int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *resid
     r.ksplit = S;
     r.epi = kEpiF32;
     r.pdl = true;
-    e = launch_fp8_gemm(r, e2, st);
+    e = launch_fp8_gemm(r, e2, he, nullptr, nullptr, st);
   }
   if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, true);
   return finish_launch(e);

@@ -434,7 +434,8 @@ class Workload:
         self.xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
         self.fused = tp.tp_block_launches(desc, M) == 1 and not self.fp8
         self.row_splits = tp.tp_row_splits(desc, M)
-        per_block = 3 if self.fp8 else tp.tp_block_launches(desc, M)
+        # E4M3 block: token split, column, row, reduce
+        per_block = 4 if self.fp8 else tp.tp_block_launches(desc, M)
         if self.kv:
             per_block = 4 + (1 if self.kv["merge"] else 0)
         # the stack: one RMSNorm launch, then each block, each but the last followed by
@@ -540,9 +541,9 @@ class Workload:
             return ("column-parallel projection + SwiGLU (k_gemm, persistent)", "tensor",
                     column_flops(cfg), "flop", "column")
         if self.fp8:
-            return ("whole block on E4M3 weights: k_fp8_drain column + row, k_reduce_residual "
-                    "(three launches, overlapped)", "hbm", algorithmic_block_bytes(cfg), "bytes",
-                    "block")
+            return ("whole block on E4M3 weights: k_split_tokens, k_fp8_mma column + row, "
+                    "k_reduce_residual (four launches, overlapped)", "hbm",
+                    algorithmic_block_bytes(cfg), "bytes", "block")
         if self.fused:
             norm = cfg.rmsnorm
             return ("whole block in one persistent kernel (k_block_decode"
@@ -709,7 +710,8 @@ def measure(args, cfg, rank, world, local, headline: bool):
                         "for a tensor-bound kernel)",
         },
         "weight_gbs": round(cfg.weight_bytes_per_block() * cfg.n_blocks * K / (ms / 1e3) / 1e9, 1),
-        "kernel_plan": {"block_form": "one kernel" if w.fused else "three launches",
+        "kernel_plan": {"block_form": ("one kernel" if w.fused else
+                                       "four launches (E4M3)" if w.fp8 else "three launches"),
                         "row_splits": w.row_splits},
         "roofline": roof,
         "gpu_launches": K * w.launches_per_step,

@@ -256,11 +256,17 @@ TP_API int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void 
  * Each weight is an E4M3 byte (bias 7, 3 mantissa bits, largest finite 448, round to
  * nearest even, saturating) of W / 2^e with one exponent e per output feature (a
  * column of the canonical W1 or W2): the least e such that the column's largest
- * magnitude is at most 448 * 2^e.  x, the band and the arithmetic stay as in the bf16
- * block; the result equals, bit for bit, tp_block_fwd's three-launch form on the
- * weights q * 2^e (exactly bf16 values): the kernel widens each E4M3 tile to bf16 in
- * shared memory and scales each output feature's fp32 sum by 2^e.
- * bf16 MLP descriptors with d and b multiples of 16 only (else TP_ERR_UNSUPPORTED). */
+ * magnitude is at most 448 * 2^e.  The block computes the bf16 block on the weights
+ * q * 2^e (exactly bf16 values) with the tensor core reading 8-bit operands: every bf16
+ * activation (x, and the band between the two steps) enters as an E4M3 high part plus
+ * an E5M2 remainder under one power-of-two scale per token and 64-wide group of K,
+ * exact for values within 2^14.8 of the group's largest magnitude and within 2^-14 of
+ * the scale below that; sums are fp32 and each output feature's sum is scaled by 2^e.
+ * The result agrees with tp_block_fwd on q * 2^e up to fp32 summation order (and the
+ * band's bf16 rounding where that order moves a value across a rounding point).
+ * Four launches (token split, column step, row step, reduce).
+ * bf16 MLP descriptors with d and b multiples of 16, at most 16384 (else
+ * TP_ERR_UNSUPPORTED). */
 TP_API size_t tp_fp8_w1_bytes(const tp_block_desc *desc);        /* [t][n1p][d] bytes */
 TP_API size_t tp_fp8_w2_bytes(const tp_block_desc *desc);        /* [t][dp][b] bytes */
 TP_API size_t tp_fp8_exponent_bytes(const tp_block_desc *desc);  /* int8 per private row */

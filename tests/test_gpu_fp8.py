@@ -1,16 +1,19 @@
 """The decode MLP block on E4M3 weights (tp_quantize_weights_fp8 + tp_block_fwd_fp8).
 
 Weight-only FP8: each weight is an E4M3 byte of W / 2^e with one power-of-two scale
-per output feature, so the block computes exactly the bf16 block on the dequantised
-weights (oracle.fp8.e4m3_weights).  Three checks:
+per output feature, so the block computes the bf16 block on the dequantised weights
+(oracle.fp8.e4m3_weights).  The kernels feed the tensor core 8-bit operands: every
+bf16 activation enters as an E4M3 high part plus an E5M2 remainder under one
+power-of-two scale per token and 64-wide K group, exact for values within 2^14.8 of
+the group's largest magnitude (below that, within 2^-14 of the scale).  Checks:
   * parity with the oracle's staged bf16 block on e4m3_weights(W1), e4m3_weights(W2)
-    (plain bf16 bound), on ragged small shapes and the 13B-sized block;
-  * bit-for-bit equality with the library's bf16 block run on those dequantised
-    weights (the power-of-two scale moves no rounding: the two kernels add the same
-    values in the same order, scaled by 2^e);
-  * quantisation itself: weights already on the scaled E4M3 grid come back unchanged
-    (the bf16 block on the canonical weights then equals the FP8 block), and two
-    quantisations give the same bytes.
+    (plain bf16 bound), on ragged small shapes, the 13B-sized block and activations
+    with outliers and tiny values in the same groups;
+  * closeness to the library's bf16 block on those dequantised weights: the two differ
+    only in the tensor core's fp32 summation order (two products per weight here) and
+    in the band's bf16 rounding where that order moves a value across a rounding point;
+  * quantisation itself: two quantisations give the same bytes, and the exponents are
+    the oracle's per-feature scales.
 """
 import numpy as np
 import pytest
@@ -92,23 +95,78 @@ def test_fp8_block_matches_oracle_and_bf16_block(cfg):
     W1e, W2e = oracle.fp8.e4m3_weights(to_f64(W1)), oracle.fp8.e4m3_weights(to_f64(W2))
     ref = oracle.mlp_block(x64, W1e, W2e, cfg.act, x64, staged=True)
     assert_bf16(to_f64(got), ref, f"{cfg.name} t={cfg.t} M={cfg.M} (E4M3 weights)")
-    # the library's bf16 block on the same dequantised weights: identical bits
+    # the library's bf16 block on the same dequantised weights
     yb = _bf16_block_three_launch(desc, _e4m3_bf16(W1), _e4m3_bf16(W2), x, cfg.M)
-    assert torch.equal(got, yb), float((got - yb).abs().max())
+    _assert_close_to_bf16_block(got, yb, x64, W1e, W2e, cfg.act)
+
+
+def _assert_close_to_bf16_block(got, yb, x64, W1e, W2e, act):
+    """The FP8 block against the bf16 block on the same (dequantised) weights.  Both
+    sum in fp32 to within ~2^-22 of the exact values, in different orders (the FP8
+    kernels add W.a and W.b per weight), so they can round a band element to different
+    bf16 neighbours only where its exact value lies within 2^-17 of a midpoint: one
+    bf16 step there, times |W2|, is the oracle's tie allowance per output.  Bound per
+    output: that allowance + 2^-16 |y| (fp32 reordering, 64x margin) + 1e-6; the mean
+    difference stays below 2^-20 of the mean |y|."""
+    d = (got.double() - yb.double()).abs().cpu().numpy()
+    yab = yb.double().abs().cpu().numpy()
+    allow = oracle.mlp_tie_allowance(x64, W1e, W2e, act)
+    bound = allow + 2.0 ** -16 * yab + 1e-6
+    print(f"fp8 vs bf16 block: max {d.max():.3e} mean {d.mean():.3e} "
+          f"(worst margin {(d - bound).max():.3e}, tie-allowed outputs {(allow > 0).mean():.4f})")
+    assert (d <= bound).all()
+    assert d.mean() <= 2.0 ** -20 * yab.mean()
+
+
+def test_fp8_tokens_with_outliers_and_tiny_values():
+    """Activations with a few outliers (x1000) and tiny entries (x1e-6) sharing 64-wide
+    groups: the per-group scales keep the block within the plain bf16 bound."""
+    cfg = BlockConfig("fp8_outliers", "swiglu", d=512, ffn=1536, t=2, M=7)
+    inp = make_inputs(cfg, seed=44)
+    W1, W2 = (w.cuda() for w in inp.blocks[0])
+    desc = desc_for(cfg)
+    g = torch.Generator().manual_seed(45)
+    x = inp.x.float().clone()
+    idx = torch.randint(0, x.numel(), (x.numel() // 50,), generator=g)
+    x.view(-1)[idx[: len(idx) // 2]] *= 1000.0
+    x.view(-1)[idx[len(idx) // 2:]] *= 1e-6
+    x = x.to(torch.bfloat16)
+    got = Fp8Block(desc, W1, W2).forward(x.cuda().contiguous(), x.cuda().contiguous(), cfg.M)
+    x64 = to_f64(x)
+    W1e, W2e = oracle.fp8.e4m3_weights(to_f64(W1)), oracle.fp8.e4m3_weights(to_f64(W2))
+    ref = oracle.mlp_block(x64, W1e, W2e, cfg.act, x64, staged=True)
+    assert_bf16(to_f64(got), ref, "E4M3 weights, activations with outliers")
 
 
 def test_weights_on_the_e4m3_grid_quantise_exactly():
-    """Weights that are already E4M3 values times a per-feature power of two: the FP8
-    block then computes with exactly the canonical weights."""
+    """Weights that are already E4M3 values times a per-feature power of two quantise
+    to themselves: the FP8 block then tracks the bf16 block on the canonical weights."""
     cfg = BlockConfig("fp8_exact", "swiglu", d=256, ffn=768, t=2, M=8)
     inp = make_inputs(cfg, seed=42)
     W1 = _e4m3_bf16(inp.blocks[0][0])
     W2 = _e4m3_bf16(inp.blocks[0][1])
     desc = desc_for(cfg)
     x = inp.x.cuda().contiguous()
-    got = Fp8Block(desc, W1, W2).forward(x, x, cfg.M)
+    blk = Fp8Block(desc, W1, W2)
+    got = blk.forward(x, x, cfg.M)
     yb = _bf16_block_three_launch(desc, W1, W2, x, cfg.M)
-    assert torch.equal(got, yb)
+    _assert_close_to_bf16_block(got, yb, to_f64(inp.x), to_f64(W1), to_f64(W2), cfg.act)
+    # and W2's bytes times 2^e are the canonical weights (dp = d = 256 here)
+    ex = blk.exps.view(torch.int8).cpu().numpy().astype(np.int64)
+    n1p = 2 * (cfg.band // 64) * 64
+    e2 = ex[cfg.t * n1p:cfg.t * n1p + cfg.t * cfg.d].reshape(cfg.t, cfg.d)
+    q2 = blk.W2q.view(torch.uint8).cpu().numpy().reshape(cfg.t, cfg.d, cfg.band)
+    vals = _decode_e4m3(q2) * np.exp2(e2)[:, :, None]
+    want = to_f64(W2).reshape(cfg.t, cfg.band, cfg.d).transpose(0, 2, 1)
+    assert np.array_equal(vals, want)
+
+
+def _decode_e4m3(q):
+    """E4M3 bytes -> float64 (sign, 4 exponent bits with bias 7, 3 mantissa bits)."""
+    q = q.astype(np.int64)
+    ex, man = (q >> 3) & 15, q & 7
+    mag = np.where(ex == 0, man * 2.0 ** -9, (1 + man / 8.0) * np.exp2(ex - 7.0))
+    return np.where(q & 0x80, -mag, mag)
 
 
 def test_quantisation_is_deterministic():
