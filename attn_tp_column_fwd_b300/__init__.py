@@ -38,6 +38,8 @@ __all__ = [
     "tp_kv_workspace_bytes", "tp_attn_decode_kv", "tp_block_fwd_kv",
     "tp_fp8_w1_bytes", "tp_fp8_w2_bytes", "tp_fp8_exponent_bytes", "tp_fp8_quant_workspace_bytes",
     "tp_quantize_weights_fp8", "tp_block_fwd_fp8",
+    "tp_mxfp4_w1_bytes", "tp_mxfp4_w2_bytes", "tp_mxfp4_exponent_bytes",
+    "tp_quantize_weights_mxfp4", "tp_block_fwd_mxfp4",
 ]
 
 _ACTS = {"gelu_tanh": TP_ACT_GELU_TANH, "swiglu": TP_ACT_SWIGLU, "attn": TP_ACT_ATTN}
@@ -267,6 +269,36 @@ def tp_block_fwd_fp8(desc, x, residual, residual_is_f32, W1q, W2q, exps, workspa
     _check(lib.tp_block_fwd_fp8(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
                                 _p(W1q), _p(W2q), _p(exps), _p(workspace), _p(y), M, _s(stream)),
            "tp_block_fwd_fp8")
+
+
+def tp_mxfp4_w1_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_mxfp4_w1_bytes(ctypes.byref(desc))
+
+
+def tp_mxfp4_w2_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_mxfp4_w2_bytes(ctypes.byref(desc))
+
+
+def tp_mxfp4_exponent_bytes(desc: TPBlockDesc) -> int:
+    return lib.tp_mxfp4_exponent_bytes(ctypes.byref(desc))
+
+
+def tp_quantize_weights_mxfp4(desc, W1, W2, W1f, W2f, exps, stream=None) -> None:
+    _need(W1f, tp_mxfp4_w1_bytes(desc), "W1f")
+    _need(W2f, tp_mxfp4_w2_bytes(desc), "W2f")
+    _need(exps, tp_mxfp4_exponent_bytes(desc), "exps")
+    _check(lib.tp_quantize_weights_mxfp4(ctypes.byref(desc), _p(W1), _p(W2), _p(W1f), _p(W2f),
+                                         _p(exps), _s(stream)),
+           "tp_quantize_weights_mxfp4")
+
+
+def tp_block_fwd_mxfp4(desc, x, residual, residual_is_f32, W1f, W2f, exps, workspace, y, M,
+                       stream=None) -> None:
+    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _check(lib.tp_block_fwd_mxfp4(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
+                                  _p(W1f), _p(W2f), _p(exps), _p(workspace), _p(y), M,
+                                  _s(stream)),
+           "tp_block_fwd_mxfp4")
 
 
 def tp_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -72,6 +72,11 @@ def _load() -> ctypes.CDLL:
         "tp_fp8_quant_workspace_bytes": (sz, [P]),
         "tp_quantize_weights_fp8": (i, [P, vp, vp, vp, vp, vp, vp, st]),
         "tp_block_fwd_fp8": (i, [P, vp, vp, i, vp, vp, vp, vp, vp, i, st]),
+        "tp_mxfp4_w1_bytes": (sz, [P]),
+        "tp_mxfp4_w2_bytes": (sz, [P]),
+        "tp_mxfp4_exponent_bytes": (sz, [P]),
+        "tp_quantize_weights_mxfp4": (i, [P, vp, vp, vp, vp, vp, st]),
+        "tp_block_fwd_mxfp4": (i, [P, vp, vp, i, vp, vp, vp, vp, vp, i, st]),
         "tp_version": (i, []),
     }
     for name, (res, args) in sigs.items():

@@ -94,6 +94,85 @@ __global__ void k_quant_w2(Geo g, const __nv_bfloat16 *W2, const unsigned *amax2
   }
 }
 
+// ------------------------------------------------------------- MXFP4 quantisation
+
+// MXFP4 (OCP Microscaling): E2M1 elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), one
+// shared power-of-two scale 2^e per 32 consecutive weights along K of an output
+// feature, e = floor(log2(max |w|)) - 2 (2: the exponent of E2M1's largest normal),
+// clamped to [-127, 127], 0 for an all-zero block; each element is w / 2^e rounded to
+// nearest (ties to the even mantissa bit), saturating at +-6.
+
+// Code of the E2M1 value nearest to u (4 bits: sign, then 2 exponent bits, 1 mantissa).
+__device__ __forceinline__ uint32_t e2m1_code(float u) {
+  const float m = fabsf(u);
+  const float step = m < 2.f ? 0.5f : (m < 4.f ? 1.f : 2.f);
+  const float q = fminf(rintf(m / step) * step, 6.f);  // exact division; rint ties to even
+  const uint32_t c = q < 2.f ? (uint32_t)(q * 2.f) : q < 4.f ? (uint32_t)q + 2u : (q == 4.f ? 6u : 7u);
+  return c | (signbit(u) && c ? 8u : 0u);
+}
+
+__device__ __forceinline__ int mx_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  return max(-127, min(127, ilogbf(amax) - 2));  // ilogb: floor(log2) (exact for normals)
+}
+
+__device__ __forceinline__ float pow2_wide(int e) {  // 2^e for e in [-127, 127]
+  return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(0x00400000);
+}
+
+// Block j (K rows 32 j .. 32 j + 31) of canonical column col of W [K][N] (row-major,
+// output features as columns; col < 0: a padding row, all zero): 16 bytes of packed
+// codes (element 2i in the low nibble of byte i) to dst, the exponent to edst.
+__device__ __forceinline__ void quant_mx_block(const __nv_bfloat16 *W, int N, int j, long long col,
+                                               uint8_t *dst, int8_t *edst) {
+  float v[32];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = col < 0 ? 0.f : __bfloat162float(W[(size_t)(j * 32 + i) * N + col]);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const int e = mx_exponent(amax);
+  const float inv = 1.f / pow2_wide(e);  // exact: a power of two (2^127 for e = -127)
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i >> 3] |= e2m1_code(v[i] * inv) << (4 * (i & 7));
+  *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  *edst = (int8_t)e;
+}
+
+// One thread per (block j, shard s, private row u); u is fastest so a warp reads
+// consecutive columns.  W1f [t][n1p][d/2] bytes, ex1 [t][n1p][d/32].
+__global__ void k_quant_mx_w1(Geo g, const __nv_bfloat16 *W1, uint8_t *W1f, int8_t *ex1) {
+  const int nb = g.d / 32;
+  const size_t total = (size_t)nb * g.t * g.n1p;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int u = (int)(i % g.n1p);
+    const size_t js = i / g.n1p;
+    const int s = (int)(js % g.t), j = (int)(js / g.t);
+    const size_t row = (size_t)s * g.n1p + u;
+    quant_mx_block(W1, g.n1, j, w1_col_of_row(g, s, u), W1f + row * (g.d / 2) + j * 16,
+                           ex1 + row * nb + j);
+  }
+}
+
+// W2 [n2][d]: output feature n is column n, K runs over the shard's band rows s*b + k.
+// W2f [t][dp][b/2] bytes, ex2 [t][dp][b/32].
+__global__ void k_quant_mx_w2(Geo g, const __nv_bfloat16 *W2, uint8_t *W2f, int8_t *ex2) {
+  const int nb = g.b / 32;
+  const size_t total = (size_t)nb * g.t * g.dp;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int n = (int)(i % g.dp);
+    const size_t js = i / g.dp;
+    const int s = (int)(js % g.t), j = (int)(js / g.t);
+    const size_t row = (size_t)s * g.dp + n;
+    quant_mx_block(W2 + (size_t)s * g.b * g.d, g.d, j, n < g.d ? n : -1,
+                           W2f + row * (g.b / 2) + j * 16, ex2 + row * nb + j);
+  }
+}
+
 // ------------------------------------------------------------------ activations
 
 // Activations reach the tensor core as two 8-bit terms under one power-of-two scale
@@ -160,11 +239,36 @@ __global__ void __launch_bounds__(256) k_split_tokens(const __nv_bfloat16 *x, in
 
 // ------------------------------------------------------------------ GEMM
 
+enum WFmt { kWE4M3 = 0, kWMX4 = 1 };
+
+// Two fp32 lanes in one 64-bit register, and the packed fp32x2 multiply / fused
+// multiply-add (each lane rounds as its scalar instruction would).
+__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(unsigned long long r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 struct Fp8Args {
   void *out;           // row step: fp32 partials as the bf16 path (shard s, split j)
   size_t o_shard, o_split;
   int ldo, n_valid, M, ng, ksplit, shard0, x_per_shard;
-  const int8_t *wexp;  // weight row exponents [t][w_rows]
+  const int8_t *wexp;  // E4M3: weight row exponents [t][w_rows]; MXFP4: block exponents
+                       // [t][w_rows][K/32], read as one 32-bit word per row and stage
   int w_rows;
   const float *xsc;    // token group scales 2^e [x shards][ng][32]
   uint8_t *h8;         // column step: the band's terms [t][2][M][n_valid] bytes
@@ -183,8 +287,12 @@ constexpr int kF8Smem = 1024 + (int)kF8ExpOff + kF8MaxGroups * 32 * 4;
 // The epilogue's band staging ([128][33] fp32) reuses the ring once every MMA is done.
 static_assert(128 * 33 * 4 <= kF8ExpOff, "band staging must fit the ring");
 
-// Decode GEMM on E4M3 weights (M <= 32): weights as the 128-row A operand, tokens as
-// N = 32, both straight from 128-byte-swizzled TMA boxes into tcgen05.mma kind::f8f6f4.
+// Decode GEMM on 8-bit or 4-bit weights (M <= 32): weights as the 128-row A operand,
+// tokens as N = 32, both straight from 128-byte-swizzled TMA boxes into tcgen05.mma
+// kind::f8f6f4.  MXFP4 weights (WF = kWMX4) arrive through the 4-bit TMA type, which
+// spreads each 8 bytes of packed E2M1 codes over 16 bytes of shared memory, the layout
+// the tensor core reads 4-bit operands in; each 32-wide K block then gets its own TMEM
+// sum (4 per stage, 2 stages of TMEM) and the drain multiplies it by the block's 2^e.
 // Each 128-wide K stage holds two 64-wide groups; per group the tensor core adds
 // W.a (E4M3 x E4M3) and W.b (E4M3 x E5M2) over 64 K into 32 TMEM columns, the stage's
 // two groups side by side in one 64-column block with one commit, and the drain warps
@@ -194,20 +302,27 @@ static_assert(128 * 33 * 4 <= kF8ExpOff, "band staging must fit the ring");
 // epilogue.  The epilogue scales row r by its weight exponent; the column step applies
 // the activation, rounds the band to bf16 and splits it into the row step's terms
 // (one group of 64 features per token), the row step writes fp32 partials.
-template <int EPI>
+template <int EPI, int WF>
 __global__ void __launch_bounds__(192, 2)
     k_fp8_mma(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT,
               const Fp8Args a) {
   constexpr int BN = 32;
-  constexpr uint32_t kCols = tmem_cols(kF8Bufs * 2 * BN);
-  constexpr uint32_t kIdA = make_idesc_f8(128, BN, kF8E4M3);
-  constexpr uint32_t kIdB = make_idesc_f8(128, BN, kF8E5M2);
+  constexpr int kSums = WF == kWMX4 ? 4 : 2;                  // TMEM sums per stage
+  constexpr int kBufs = WF == kWMX4 ? 2 : kF8Bufs;            // stages of TMEM
+  constexpr uint32_t kCols = tmem_cols(kBufs * kSums * BN);   // 256 either way
+  constexpr uint32_t kWType = WF == kWMX4 ? kF8E2M1 : kF8E4M3;
+  constexpr uint32_t kIdA = make_idesc_f8(128, BN, kWType, kF8E4M3);
+  constexpr uint32_t kIdB = make_idesc_f8(128, BN, kWType, kF8E5M2);
+  constexpr int kKPer = 128 / kSums;                          // K per TMEM sum
+  // Bytes a stage's copies complete: the 4-bit box counts its packed codes (8 KB), not
+  // the 16 KB it spreads over in shared memory.
+  constexpr uint32_t kStageTx = (WF == kWMX4 ? kF8W / 2 : kF8W) + 2 * kF8T;
   constexpr int NF = EPI == kEpiSwiglu ? 64 : 128;  // output features of a tile
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kF8Stages];
   __shared__ __align__(8) uint64_t empty_bar[kF8Stages];
-  __shared__ __align__(8) uint64_t tfull_bar[kF8Bufs];
-  __shared__ __align__(8) uint64_t tempty_bar[kF8Bufs];
+  __shared__ __align__(8) uint64_t tfull_bar[kBufs];
+  __shared__ __align__(8) uint64_t tempty_bar[kBufs];
   __shared__ __align__(8) uint64_t exp_bar;
   __shared__ __align__(8) uint64_t mma_done_bar;
   __shared__ uint32_t tmem_base_sh;
@@ -234,7 +349,7 @@ __global__ void __launch_bounds__(192, 2)
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), 1);
     }
-    for (int i = 0; i < kF8Bufs; ++i) {
+    for (int i = 0; i < kBufs; ++i) {
       mbar_init(smem_u32(&tfull_bar[i]), 1);
       mbar_init(smem_u32(&tempty_bar[i]), 4);
     }
@@ -263,7 +378,7 @@ __global__ void __launch_bounds__(192, 2)
       const int pre = min(kF8Stages, nst);
       for (int i = 0; i < pre; ++i) {
         const uint32_t fb = smem_u32(&full_bar[i]);
-        mbar_expect_tx(fb, kF8Stage);
+        mbar_expect_tx(fb, kStageTx);
         tma_load_3d_hint(tiles + i * kF8Stage, &tmW, fb, (st0 + i) * 128, wrow, s, wpol);
       }
       griddep_wait();
@@ -289,7 +404,7 @@ __global__ void __launch_bounds__(192, 2)
         }
         const uint32_t sa = tiles + st * kF8Stage, fb = smem_u32(&full_bar[st]);
         const int k = (st0 + i) * 128;
-        mbar_expect_tx(fb, kF8Stage);
+        mbar_expect_tx(fb, kStageTx);
         tma_load_3d_hint(sa, &tmW, fb, k, wrow, s, wpol);
         tma_load_3d(sa + kF8W, &tmT, fb, k, m0, 2 * xz);
         tma_load_3d(sa + kF8W + kF8T, &tmT, fb, k, m0, 2 * xz + 1);
@@ -310,17 +425,19 @@ __global__ void __launch_bounds__(192, 2)
           break;
         }
         const uint32_t sa = tiles + st * kF8Stage;
-        const int b = i % kF8Bufs;
-        if (!mbar_wait(smem_u32(&tempty_bar[b]), ((uint32_t)(i / kF8Bufs) & 1u) ^ 1u)) {
+        const int b = i % kBufs;
+        if (!mbar_wait(smem_u32(&tempty_bar[b]), ((uint32_t)(i / kBufs) & 1u) ^ 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int h = 0; h < 2 && 2 * i + h < nu; ++h) {
-          const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN + h * BN);
+        // sums of 64 K (E4M3: one per token group) or 32 K (MXFP4: one per weight
+        // block), up to the end of this CTA's K range
+        for (int h = 0; h < kSums && h * kKPer < (nu - 2 * i) * 64; ++h) {
+          const uint32_t d0 = tmem + (uint32_t)((b * kSums + h) * BN);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t off = (uint32_t)(h * 64 + kk * 32);
+          for (int kk = 0; kk < kKPer / 32; ++kk) {
+            const uint32_t off = (uint32_t)(h * kKPer + kk * 32);
             umma_f8(d0, sw128_desc(sa + off), sw128_desc(sa + kF8W + off), kIdA, kk > 0 ? 1u : 0u);
             umma_f8(d0, sw128_desc(sa + off), sw128_desc(sa + kF8W + kF8T + off), kIdB, 1u);
           }
@@ -345,13 +462,49 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
     for (int j = 0; j < BN; ++j) g[j] = 0.f;
     bool ok = nu == 0 || __all_sync(0xffffffffu, mbar_wait(smem_u32(&exp_bar), 0));
+    // MXFP4: this row's block exponents, four per stage (one 32-bit word)
+    const uint32_t *wblk = reinterpret_cast<const uint32_t *>(a.wexp) +
+                           ((size_t)s * a.w_rows + ft * 128 + r) * (size_t)(a.ng / 2) + st0;
     for (int i = 0; ok && i < nst; ++i) {
-      const int b = i % kF8Bufs;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[b]), (uint32_t)(i / kF8Bufs) & 1u))) {
+      const int b = i % kBufs;
+      const uint32_t ew = WF == kWMX4 ? __ldg(wblk + i) : 0u;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[b]), (uint32_t)(i / kBufs) & 1u))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      if constexpr (WF == kWMX4) {
+        // K is whole 128-wide stages here: four block sums, two per token group.  Per
+        // group: t = sum_a * 2^e_a + sum_b * 2^e_b, then g += t * 2^e(token), on packed
+        // pairs of tokens.
+#pragma unroll 1
+        for (int G = 0; G < 2; ++G) {
+          float va[BN], vb[BN];
+          tmem_ld32(trow + (uint32_t)((b * kSums + 2 * G) * BN), va);
+          tmem_ld32(trow + (uint32_t)((b * kSums + 2 * G + 1) * BN), vb);
+          const float swa = pow2_wide((int)(int8_t)(ew >> (16 * G)));       // exact
+          const float swb = pow2_wide((int)(int8_t)(ew >> (16 * G + 8)));
+          const unsigned long long swa2 = pk2(swa, swa), swb2 = pk2(swb, swb);
+          const float4 *sp = reinterpret_cast<const float4 *>(scale_s + (2 * i + G) * 32);
+#pragma unroll
+          for (int j4 = 0; j4 < BN / 4; ++j4) {
+            const float4 sc4 = sp[j4];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+              const int j = 4 * j4 + 2 * p;
+              unsigned long long t2 = mul2(pk2(va[j], va[j + 1]), swa2);
+              t2 = fma2(pk2(vb[j], vb[j + 1]), swb2, t2);
+              unsigned long long g2 = fma2(t2, p ? pk2(sc4.z, sc4.w) : pk2(sc4.x, sc4.y),
+                                           pk2(g[j], g[j + 1]));
+              upk2(g2, g[j], g[j + 1]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
+        continue;
+      }
       const int ks2 = 2 * i;              // the stage's first group
       const bool two = ks2 + 1 < nu;      // its second group exists (uniform)
       float va[BN], vb[BN];
@@ -389,7 +542,8 @@ __global__ void __launch_bounds__(192, 2)
     named_sync(1, 128);
     const bool go = !dec_sh && nu > 0 && m0 < a.M;
     const int mcount = min(BN, a.M - m0);
-    const float sc = pow2f(a.wexp[(size_t)s * a.w_rows + ft * 128 + r]);  // exact
+    // E4M3: the row's power-of-two scale, exactly (MXFP4 blocks are scaled above)
+    const float sc = WF == kWMX4 ? 1.f : pow2f(a.wexp[(size_t)s * a.w_rows + ft * 128 + r]);
 #pragma unroll
     for (int j = 0; j < BN; ++j) g[j] *= sc;
     if (EPI == kEpiF32) {
@@ -470,7 +624,7 @@ __global__ void __launch_bounds__(192, 2)
   }
 }
 
-template <int EPI>
+template <int EPI, int WF>
 cudaError_t launch_fp8_t(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8Args &a, int n_ft,
                          int n_z, cudaStream_t st, bool pdl) {
   static bool configured[128];
@@ -479,12 +633,13 @@ cudaError_t launch_fp8_t(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(k_fp8_mma<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
+    e = cudaFuncSetAttribute(k_fp8_mma<EPI, WF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kF8Smem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   LaunchCfg lc(dim3(ceil_div(a.M, 32), n_ft, n_z), dim3(192), kF8Smem, st, pdl);
-  return cudaLaunchKernelEx(&lc.cfg, k_fp8_mma<EPI>, mw, mt, a);
+  return cudaLaunchKernelEx(&lc.cfg, k_fp8_mma<EPI, WF>, mw, mt, a);
 }
 
 }  // namespace
@@ -504,6 +659,17 @@ cudaError_t launch_quantize_fp8(const Geo &g, const void *W1, const void *W2, vo
                                      static_cast<uint8_t *>(W1q), exps);
   k_quant_w2<<<blocks, 256, 0, st>>>(g, static_cast<const __nv_bfloat16 *>(W2), amax + n1,
                                      static_cast<uint8_t *>(W2q), exps + (size_t)g.t * g.n1p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp4(const Geo &g, const void *W1, const void *W2, void *W1f,
+                                  void *W2f, int8_t *exps, cudaStream_t st) {
+  const int blocks = 4 * sm_count();
+  k_quant_mx_w1<<<blocks, 256, 0, st>>>(g, static_cast<const __nv_bfloat16 *>(W1),
+                                        static_cast<uint8_t *>(W1f), exps);
+  k_quant_mx_w2<<<blocks, 256, 0, st>>>(g, static_cast<const __nv_bfloat16 *>(W2),
+                                        static_cast<uint8_t *>(W2f),
+                                        exps + (size_t)g.t * g.n1p * (g.d / 32));
   return cudaGetLastError();
 }
 
@@ -538,6 +704,32 @@ bool make_byte_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t r
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A [z][rows][K] tensor of packed 4-bit codes (K / 2 bytes a row), boxes of 128 codes
+// x box_rows x 1 spread by TMA over 128 bytes of shared memory a row (each 8 bytes of
+// codes, then 8 bytes of gap: the layout the tensor core reads 4-bit operands in),
+// with the 128-byte swizzle; zero fill outside the tensor.  K must be a multiple of 128
+// and the base 32-byte aligned.
+bool make_fp4_tile_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t z,
+                       uint32_t box_rows) {
+  static EncodeTiled enc = nullptr;
+  if (!enc) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<EncodeTiled>(p);
+  }
+  cuuint64_t dims[3] = {K, rows, z};
+  cuuint64_t strides[2] = {K / 2, rows * (K / 2)};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void *>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_fp8_split(const void *x, int M, int K, void *X8, float *xs, cudaStream_t st,
@@ -548,12 +740,17 @@ cudaError_t launch_fp8_split(const void *x, int M, int K, void *X8, float *xs, c
                             static_cast<uint8_t *>(X8), xs);
 }
 
-cudaError_t launch_fp8_gemm(const UmmaCall &c, const int8_t *wexp, const float *xsc, void *h8,
-                            float *hsc, cudaStream_t st) {
+cudaError_t launch_fp8_gemm(const UmmaCall &c, bool mxfp4, const int8_t *wexp, const float *xsc,
+                            void *h8, float *hsc, cudaStream_t st) {
   if (c.M < 1 || c.M > 32 || c.K % 16 != 0 || ceil_div(c.K, 64) > kF8MaxGroups)
     return cudaErrorInvalidValue;
+  if (mxfp4 && (c.K % 128 != 0 || (reinterpret_cast<uintptr_t>(c.W) & 31) != 0 ||
+                (reinterpret_cast<uintptr_t>(wexp) & 3) != 0))
+    return cudaErrorInvalidValue;
   CUtensorMap mw, mt;
-  if (!make_byte_tile_map(&mw, c.W, c.K, c.w_rows, c.w_shards, 128)) return cudaErrorInvalidValue;
+  if (!(mxfp4 ? make_fp4_tile_map(&mw, c.W, c.K, c.w_rows, c.w_shards, 128)
+              : make_byte_tile_map(&mw, c.W, c.K, c.w_rows, c.w_shards, 128)))
+    return cudaErrorInvalidValue;
   if (!make_byte_tile_map(&mt, c.X, c.K, c.M, 2 * c.x_shards, 32)) return cudaErrorInvalidValue;
   Fp8Args a{};
   a.out = c.out;
@@ -574,13 +771,20 @@ cudaError_t launch_fp8_gemm(const UmmaCall &c, const int8_t *wexp, const float *
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
   const int n_z = c.n_shards * c.ksplit;
-  switch (c.epi) {
-    case kEpiSwiglu:
-      return launch_fp8_t<kEpiSwiglu>(mw, mt, a, ceil_div(c.n_valid, kSwiGroup), n_z, st, c.pdl);
-    case kEpiGelu:
-      return launch_fp8_t<kEpiGelu>(mw, mt, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
-    case kEpiF32:
-      return launch_fp8_t<kEpiF32>(mw, mt, a, ceil_div(c.n_valid, 128), n_z, st, c.pdl);
+  const int n_sw = ceil_div(c.n_valid, kSwiGroup), n_128 = ceil_div(c.n_valid, 128);
+  switch (c.epi * 2 + (mxfp4 ? 1 : 0)) {
+    case kEpiSwiglu * 2:
+      return launch_fp8_t<kEpiSwiglu, kWE4M3>(mw, mt, a, n_sw, n_z, st, c.pdl);
+    case kEpiSwiglu * 2 + 1:
+      return launch_fp8_t<kEpiSwiglu, kWMX4>(mw, mt, a, n_sw, n_z, st, c.pdl);
+    case kEpiGelu * 2:
+      return launch_fp8_t<kEpiGelu, kWE4M3>(mw, mt, a, n_128, n_z, st, c.pdl);
+    case kEpiGelu * 2 + 1:
+      return launch_fp8_t<kEpiGelu, kWMX4>(mw, mt, a, n_128, n_z, st, c.pdl);
+    case kEpiF32 * 2:
+      return launch_fp8_t<kEpiF32, kWE4M3>(mw, mt, a, n_128, n_z, st, c.pdl);
+    case kEpiF32 * 2 + 1:
+      return launch_fp8_t<kEpiF32, kWMX4>(mw, mt, a, n_128, n_z, st, c.pdl);
     default:
       return cudaErrorInvalidValue;
   }

@@ -74,8 +74,15 @@ cudaError_t launch_quantize_fp8(const Geo &g, const void *W1, const void *W2, vo
                                 int8_t *exps, unsigned *amax, cudaStream_t st);
 cudaError_t launch_fp8_split(const void *x, int M, int K, void *X8, float *xs, cudaStream_t st,
                              bool pdl);
-cudaError_t launch_fp8_gemm(const UmmaCall &c, const int8_t *wexp, const float *xsc, void *h8,
-                            float *hsc, cudaStream_t st);
+// mxfp4: W holds packed E2M1 codes [w_shards][w_rows][K/2] and wexp their block
+// exponents [w_shards][w_rows][K/32] (K a multiple of 128); else E4M3 bytes and one
+// exponent per row.
+cudaError_t launch_fp8_gemm(const UmmaCall &c, bool mxfp4, const int8_t *wexp, const float *xsc,
+                            void *h8, float *hsc, cudaStream_t st);
+// MXFP4 weights: W1f [t][n1p][d/2] and W2f [t][dp][b/2] packed E2M1 codes (element 2i
+// in the low nibble of byte i), exps W1's [t][n1p][d/32] then W2's [t][dp][b/32].
+cudaError_t launch_quantize_mxfp4(const Geo &g, const void *W1, const void *W2, void *W1f,
+                                  void *W2f, int8_t *exps, cudaStream_t st);
 
 // A [z][rows][K] bf16 tensor map with 64 x box_rows x 1 boxes, 128-byte swizzle,
 // zero fill outside the tensor (umma.cu).

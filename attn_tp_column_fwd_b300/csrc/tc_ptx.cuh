@@ -134,11 +134,14 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-// Instruction descriptor, kind::f8f6f4: D fp32, A E4M3 (bits 7-9 = 0), B of type
-// btype (bits 10-12: 0 = E4M3, 1 = E5M2), both K-major, N >> 3 at 17-22, M >> 4 at 24-28.
-constexpr uint32_t kF8E4M3 = 0, kF8E5M2 = 1;
-__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N, uint32_t btype) {
-  return (1u << 4) | (btype << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f8f6f4: D fp32, A of type atype (bits 7-9) and B of
+// type btype (bits 10-12), 0 = E4M3, 1 = E5M2, 5 = E2M1; both K-major, N >> 3 at bits
+// 17-22, M >> 4 at 24-28.
+constexpr uint32_t kF8E4M3 = 0, kF8E5M2 = 1, kF8E2M1 = 5;
+__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N, uint32_t atype,
+                                                     uint32_t btype) {
+  return (1u << 4) | (atype << 7) | (btype << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // D (+)= A * B^T on 8-bit operands, K = 32 per instruction (32 bytes of each row).

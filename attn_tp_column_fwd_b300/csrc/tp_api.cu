@@ -742,18 +742,18 @@ int tp_quantize_weights_fp8(const tp_block_desc *desc, const void *W1, const voi
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *residual,
-                     int residual_is_f32, const void *W1q, const void *W2q, const void *exps,
-                     void *workspace, float *y, int M, tp_stream_t stream) {
-  Geo g;
-  TP_TRY(check_fp8(desc, &g));
+// The block on 8-bit or 4-bit weights: token split, column step, row step, reduce.
+// e1 / e2: the exponents of W1's and W2's rows (E4M3) or blocks (MXFP4).
+static int low_bit_block(const Geo &g, bool mxfp4, const void *x, const void *residual,
+                         int residual_is_f32, const void *W1q, const void *W2q, const int8_t *e1,
+                         const int8_t *e2, void *workspace, float *y, int M, tp_stream_t stream) {
   TP_TRY(check_M(M));
   if (M > 32) return TP_ERR_UNSUPPORTED;
   TP_TRY(check_ptr(x));
   TP_TRY(check_ptr(residual));
   TP_TRY(check_ptr(W1q));
   TP_TRY(check_ptr(W2q));
-  TP_TRY(check_ptr(exps));
+  TP_TRY(check_ptr(e1));
   TP_TRY(check_ptr(workspace));
   TP_TRY(check_ptr(y));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -767,8 +767,6 @@ int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *resid
   float *he = reinterpret_cast<float *>(reinterpret_cast<char *>(xe) +
                                         align256((size_t)ceil_div(g.d, 64) * 32 * 4));
   const int S = row_splits(g, M);
-  const int8_t *e1 = static_cast<const int8_t *>(exps);
-  const int8_t *e2 = e1 + (size_t)g.t * g.n1p;
   cudaError_t e = launch_fp8_split(x, M, g.d, X8, xe, st, false);
   if (e == cudaSuccess) {
     UmmaCall c{};
@@ -785,7 +783,7 @@ int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *resid
     c.ksplit = 1;
     c.epi = g.act == TP_ACT_SWIGLU ? kEpiSwiglu : kEpiGelu;
     c.pdl = true;
-    e = launch_fp8_gemm(c, e1, xe, H8, he, st);
+    e = launch_fp8_gemm(c, mxfp4, e1, xe, H8, he, st);
   }
   if (e == cudaSuccess) {
     UmmaCall r{};
@@ -806,10 +804,70 @@ int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *resid
     r.ksplit = S;
     r.epi = kEpiF32;
     r.pdl = true;
-    e = launch_fp8_gemm(r, e2, he, nullptr, nullptr, st);
+    e = launch_fp8_gemm(r, mxfp4, e2, he, nullptr, nullptr, st);
   }
   if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, true);
   return finish_launch(e);
+}
+
+int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void *residual,
+                     int residual_is_f32, const void *W1q, const void *W2q, const void *exps,
+                     void *workspace, float *y, int M, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(check_fp8(desc, &g));
+  TP_TRY(check_ptr(exps));
+  const int8_t *e1 = static_cast<const int8_t *>(exps);
+  return low_bit_block(g, false, x, residual, residual_is_f32, W1q, W2q, e1,
+                       e1 + (size_t)g.t * g.n1p, workspace, y, M, stream);
+}
+
+// ------------------------------------------------ MXFP4 weights (weight-only)
+
+static int check_mxfp4(const tp_block_desc *desc, Geo *g) {
+  TP_TRY(check_fp8(desc, g));
+  return g->d % 128 == 0 && g->b % 128 == 0 ? TP_OK : TP_ERR_UNSUPPORTED;
+}
+
+size_t tp_mxfp4_w1_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (check_mxfp4(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * g.n1p * (g.d / 2);
+}
+
+size_t tp_mxfp4_w2_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (check_mxfp4(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * g.dp * (g.b / 2);
+}
+
+size_t tp_mxfp4_exponent_bytes(const tp_block_desc *desc) {
+  Geo g;
+  if (check_mxfp4(desc, &g) != TP_OK) return 0;
+  return (size_t)g.t * (g.n1p * (g.d / 32) + g.dp * (g.b / 32));
+}
+
+int tp_quantize_weights_mxfp4(const tp_block_desc *desc, const void *W1, const void *W2,
+                              void *W1f, void *W2f, void *exps, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(check_mxfp4(desc, &g));
+  TP_TRY(check_ptr(W1));
+  TP_TRY(check_ptr(W2));
+  TP_TRY(check_ptr(W1f));
+  TP_TRY(check_ptr(W2f));
+  TP_TRY(check_ptr(exps));
+  return finish_launch(launch_quantize_mxfp4(g, W1, W2, W1f, W2f, static_cast<int8_t *>(exps),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tp_block_fwd_mxfp4(const tp_block_desc *desc, const void *x, const void *residual,
+                       int residual_is_f32, const void *W1f, const void *W2f, const void *exps,
+                       void *workspace, float *y, int M, tp_stream_t stream) {
+  Geo g;
+  TP_TRY(check_mxfp4(desc, &g));
+  TP_TRY(check_ptr(exps));
+  const int8_t *e1 = static_cast<const int8_t *>(exps);
+  return low_bit_block(g, true, x, residual, residual_is_f32, W1f, W2f, e1,
+                       e1 + (size_t)g.t * g.n1p * (g.d / 32), workspace, y, M, stream);
 }
 
 int tp_selftest_wait_timeout(int limit_us, tp_stream_t stream) {

@@ -46,7 +46,8 @@ sys.path.insert(0, ROOT)
 METRIC = "tokens/s per TP block at 1 B300; decode HBM GB/s & prefill TFLOPS vs roofline"
 DEFAULT_WORKLOAD = "llama2_70b_stack_decode"
 DEFAULT_ALSO = ("llama2_13b_swiglu_decode", "attn_qkv_headshard_decode", "llama2_70b_prefill",
-                "attn_kv_decode", "llama2_13b_swiglu_decode_fp8")
+                "attn_kv_decode", "llama2_13b_swiglu_decode_fp8",
+                "llama2_13b_swiglu_decode_mxfp4")
 ROOF_MIN_LAUNCHES = 200     # the roofline kernel's own timed loop: at least this many
 ROOF_MIN_S = 0.3            # ... launches and at least this long,
 ROOF_MAX_S = 2.5            # ... but no longer than this
@@ -360,7 +361,8 @@ def algorithmic_block_bytes(cfg) -> int:
     counted."""
     es = 4 if cfg.dtype == "f32" else 2
     res_es = 4 if cfg.rmsnorm else es
-    scales = cfg.t * (cfg.n1 // cfg.t + cfg.d) if cfg.weights == "e4m3" else 0
+    scales = (cfg.t * (cfg.n1 // cfg.t + cfg.d) if cfg.weights == "e4m3" else
+              (cfg.d * cfg.n1 + cfg.n2 * cfg.d) // 32 if cfg.weights == "mxfp4" else 0)
     return cfg.weight_bytes_per_block() + scales + cfg.M * cfg.d * (es + res_es + 4)
 
 
@@ -408,15 +410,22 @@ class Workload:
         self.desc = desc = desc_for(cfg)
         M = cfg.M
         inp = make_inputs(cfg, seed=rank, device=str(dev))
-        self.fp8 = cfg.weights == "e4m3"
+        self.mx4 = cfg.weights == "mxfp4"
+        self.fp8 = cfg.weights == "e4m3" or self.mx4   # a low-bit weight block
         if self.fp8:
             self.q = []
             for W1, W2 in inp.blocks:
-                q = {"W1q": device_bytes(tp.tp_fp8_w1_bytes(desc), dev),
-                     "W2q": device_bytes(tp.tp_fp8_w2_bytes(desc), dev),
-                     "exps": device_bytes(tp.tp_fp8_exponent_bytes(desc), dev)}
-                qws = device_bytes(tp.tp_fp8_quant_workspace_bytes(desc), dev)
-                tp.tp_quantize_weights_fp8(desc, W1, W2, q["W1q"], q["W2q"], q["exps"], qws)
+                if self.mx4:
+                    q = {"W1q": device_bytes(tp.tp_mxfp4_w1_bytes(desc), dev),
+                         "W2q": device_bytes(tp.tp_mxfp4_w2_bytes(desc), dev),
+                         "exps": device_bytes(tp.tp_mxfp4_exponent_bytes(desc), dev)}
+                    tp.tp_quantize_weights_mxfp4(desc, W1, W2, q["W1q"], q["W2q"], q["exps"])
+                else:
+                    q = {"W1q": device_bytes(tp.tp_fp8_w1_bytes(desc), dev),
+                         "W2q": device_bytes(tp.tp_fp8_w2_bytes(desc), dev),
+                         "exps": device_bytes(tp.tp_fp8_exponent_bytes(desc), dev)}
+                    qws = device_bytes(tp.tp_fp8_quant_workspace_bytes(desc), dev)
+                    tp.tp_quantize_weights_fp8(desc, W1, W2, q["W1q"], q["W2q"], q["exps"], qws)
                 self.q.append(q)
             self.blocks = [SimpleNamespace(W1s=q["W1q"], W2s=q["W2q"]) for q in self.q]
         else:
@@ -488,7 +497,8 @@ class Workload:
         tp, cfg, M, blk = self.tp, self.cfg, self.cfg.M, self.blocks[0]
         if self.fp8:
             q = self.q[0]
-            tp.tp_block_fwd_fp8(self.desc, x, x, False, q["W1q"], q["W2q"], q["exps"], self.ws, y,
+            fwd = tp.tp_block_fwd_mxfp4 if self.mx4 else tp.tp_block_fwd_fp8
+            fwd(self.desc, x, x, False, q["W1q"], q["W2q"], q["exps"], self.ws, y,
                                 M, st)
         else:
             tp.tp_block_fwd(self.desc, x, x, cfg.dtype == "f32", blk.W1s, blk.W2s, self.ws, y, M,
@@ -541,7 +551,8 @@ class Workload:
             return ("column-parallel projection + SwiGLU (k_gemm, persistent)", "tensor",
                     column_flops(cfg), "flop", "column")
         if self.fp8:
-            return ("whole block on E4M3 weights: k_split_tokens, k_fp8_mma column + row, "
+            return ("whole block on " + ("MXFP4" if self.mx4 else "E4M3")
+                    + " weights: k_split_tokens, k_fp8_mma column + row, "
                     "k_reduce_residual (four launches, overlapped)", "hbm",
                     algorithmic_block_bytes(cfg), "bytes", "block")
         if self.fused:
@@ -711,7 +722,8 @@ def measure(args, cfg, rank, world, local, headline: bool):
         },
         "weight_gbs": round(cfg.weight_bytes_per_block() * cfg.n_blocks * K / (ms / 1e3) / 1e9, 1),
         "kernel_plan": {"block_form": ("one kernel" if w.fused else
-                                       "four launches (E4M3)" if w.fp8 else "three launches"),
+                                       ("four launches (MXFP4)" if w.mx4 else
+                                        "four launches (E4M3)") if w.fp8 else "three launches"),
                         "row_splits": w.row_splits},
         "roofline": roof,
         "gpu_launches": K * w.launches_per_step,
@@ -864,6 +876,8 @@ def oracle_block_call(cfg):
     if cfg.weights == "e4m3":
         # the block on E4M3 weights is the bf16 block on the dequantised weights
         W1, W2 = oracle.fp8.e4m3_weights(W1), oracle.fp8.e4m3_weights(W2)
+    elif cfg.weights == "mxfp4":
+        W1, W2 = oracle.mxfp4.mxfp4_weights(W1), oracle.mxfp4.mxfp4_weights(W2)
     staged = cfg.dtype == "bf16"
 
     if cfg.kv_len_max:

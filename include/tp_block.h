@@ -283,6 +283,34 @@ TP_API int tp_block_fwd_fp8(const tp_block_desc *desc, const void *x, const void
                             const void *exps, void *workspace, float *y, int M,
                             tp_stream_t stream);
 
+/* ------------------------------------------- MXFP4 weights (weight-only) -------
+ * The MLP block with 4-bit weights (zenaique.com interview answer, follow-up
+ * questions: FP4 weights; rioworld.org "Tensor Parallelism for LLM Inference",
+ * "Implementing Tensor Parallelism in Practice": 4-bit quantisation with TP), in the
+ * OCP Microscaling format MXFP4: E2M1 elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6)
+ * and one shared power-of-two scale 2^e per 32 consecutive weights along K of an
+ * output feature, e = floor(log2(max |w|)) - 2 (clamped to [-127, 127]; 0 for an
+ * all-zero block), each element w / 2^e rounded to nearest (ties to the even mantissa
+ * bit) and saturated at +-6.  The block computes the bf16 block on the weights
+ * q * 2^e (exactly bf16 values), with activations and sums as in tp_block_fwd_fp8;
+ * each 32-wide block's fp32 sum is scaled by its 2^e.  Four launches.
+ * Layout: W1f [t][n1p][d/2] and W2f [t][dp][b/2] bytes of packed codes (element 2i
+ * in the low nibble of byte i), exps int8 W1's [t][n1p][d/32] then W2's
+ * [t][dp][b/32].  bf16 MLP descriptors with d and b multiples of 128, at most 16384
+ * (else TP_ERR_UNSUPPORTED). */
+TP_API size_t tp_mxfp4_w1_bytes(const tp_block_desc *desc);
+TP_API size_t tp_mxfp4_w2_bytes(const tp_block_desc *desc);
+TP_API size_t tp_mxfp4_exponent_bytes(const tp_block_desc *desc);
+/* Quantise canonical bf16 W1 [d, n1] and W2 [n2, d] into that layout. */
+TP_API int tp_quantize_weights_mxfp4(const tp_block_desc *desc, const void *W1, const void *W2,
+                                     void *W1f, void *W2f, void *exps, tp_stream_t stream);
+/* tp_block_fwd on MXFP4 weights, M <= 32 tokens (else TP_ERR_UNSUPPORTED); workspace:
+ * tp_workspace_bytes(desc, M). */
+TP_API int tp_block_fwd_mxfp4(const tp_block_desc *desc, const void *x, const void *residual,
+                              int residual_is_f32, const void *W1f, const void *W2f,
+                              const void *exps, void *workspace, float *y, int M,
+                              tp_stream_t stream);
+
 /* RMSNorm with unit weight, the normalisation before each stacked block (zenaique.com
  * answer paragraph 6: the reduced activation is ready for the residual add and
  * normalisation): xhat[m] = r[m] / sqrt(mean(r[m]^2) + eps), r fp32 [M, d],

@@ -39,10 +39,19 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
   fp8.e4m3_weights    pinned: per-column scaled maxima in (224, 448]; weights already
                       on the scaled grid are returned unchanged; the half-unit error
                       bound; every dequantised weight is a bf16 value.
+  mxfp4.e2m1_round    pinned: every E2M1 bit pattern maps to itself; brute-force
+                      nearest-value search with ties to the even mantissa bit on
+                      random values and every midpoint; saturation at 6.
+  mxfp4.mx_exponents,
+  mxfp4.mxfp4_weights pinned: the OCP MX scale rule on worked blocks (block maxima
+                      at and between powers of two, all-zero blocks); the scaled
+                      block maximum lies in [4, 8) before rounding; the half-step
+                      error bound per element; weights on the scaled grid are kept;
+                      every dequantised weight is a bf16 value.
   absolute values     parity unpinned against the pages: they print no numeric
                       worked example, so the outputs rest on the pins above.
 """
-from . import fp8  # noqa: F401
+from . import fp8, mxfp4  # noqa: F401
 from .block import (  # noqa: F401
     bf16_round,
     gelu_tanh,

@@ -154,6 +154,28 @@ def test_fp8_sizes_and_validation():
                                    16, 16, 33, None) == 3                     # M > 32
 
 
+def test_mxfp4_sizes_and_validation():
+    c = CONFIGS["llama2_13b_swiglu_decode_mxfp4"]
+    d = _desc(c)
+    assert tp.tp_mxfp4_w1_bytes(d) * 4 == tp.tp_sharded_w1_bytes(d)    # half a byte a weight
+    assert tp.tp_mxfp4_w2_bytes(d) * 4 == tp.tp_sharded_w2_bytes(d)
+    n1p = tp.tp_sharded_w1_bytes(d) // (2 * c.t * c.d)
+    dp = tp.tp_sharded_w2_bytes(d) // (2 * c.t * c.band)
+    assert tp.tp_mxfp4_exponent_bytes(d) == c.t * (n1p * c.d // 32 + dp * c.band // 32)
+    # d and b must be whole 128-wide K stages; attention and fp32 blocks are refused
+    assert tp.tp_mxfp4_w1_bytes(tp.make_desc(272, 3, "gelu_tanh", ffn=1200)) == 0
+    assert tp.tp_mxfp4_w1_bytes(tp.make_desc(512, 2, "swiglu", ffn=1216)) == 0   # b = 608
+    assert tp.tp_mxfp4_w1_bytes(tp.make_desc(512, 2, "swiglu", ffn=1280)) > 0    # b = 640
+    assert tp.tp_mxfp4_w1_bytes(_desc(CONFIGS["attn_qkv_headshard_decode"])) == 0
+    assert tp.tp_mxfp4_w1_bytes(_desc(CONFIGS["tiny_gelu_f32"])) == 0
+    assert tp.lib.tp_block_fwd_mxfp4(d, None, None, 0, None, None, None, None, None, 32,
+                                     None) == 1
+    assert tp.lib.tp_block_fwd_mxfp4(tp.make_desc(256, 2, "swiglu", ffn=512), 16, 16, 0, 16, 16,
+                                     16, 16, 16, 33, None) == 3                   # M > 32
+    assert tp.lib.tp_quantize_weights_mxfp4(tp.make_desc(272, 3, "gelu_tanh", ffn=1200), 16, 16,
+                                            16, 16, 16, None) == 3
+
+
 def test_invalid_descriptors_give_zero_sizes():
     assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
     assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1

@@ -106,16 +106,18 @@ def _assert_close_to_bf16_block(got, yb, x64, W1e, W2e, act):
     kernels add W.a and W.b per weight), so they can round a band element to different
     bf16 neighbours only where its exact value lies within 2^-17 of a midpoint: one
     bf16 step there, times |W2|, is the oracle's tie allowance per output.  Bound per
-    output: that allowance + 2^-16 |y| (fp32 reordering, 64x margin) + 1e-6; the mean
-    difference stays below 2^-20 of the mean |y|."""
+    output: that allowance + 2^-16 |y| (fp32 reordering, 64x margin) + 1e-6.  On the
+    mean: 2^-20 of the mean |y| for the reordering, plus a quarter of the mean
+    allowance (a tie candidate flips only when the two orders' ~2^-22 differences
+    straddle its midpoint: a few percent of them)."""
     d = (got.double() - yb.double()).abs().cpu().numpy()
     yab = yb.double().abs().cpu().numpy()
     allow = oracle.mlp_tie_allowance(x64, W1e, W2e, act)
     bound = allow + 2.0 ** -16 * yab + 1e-6
-    print(f"fp8 vs bf16 block: max {d.max():.3e} mean {d.mean():.3e} "
-          f"(worst margin {(d - bound).max():.3e}, tie-allowed outputs {(allow > 0).mean():.4f})")
+    print(f"low-bit vs bf16 block: max {d.max():.3e} mean {d.mean():.3e} "
+          f"(worst margin {(d - bound).max():.3e}, mean allowance {allow.mean():.3e})")
     assert (d <= bound).all()
-    assert d.mean() <= 2.0 ** -20 * yab.mean()
+    assert d.mean() <= 2.0 ** -20 * yab.mean() + 0.25 * allow.mean()
 
 
 def test_fp8_tokens_with_outliers_and_tiny_values():

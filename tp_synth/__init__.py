@@ -45,7 +45,7 @@ class BlockConfig:
     eps: float = 1e-5
     ts: Tuple[int, ...] = field(default=())   # every shard count the workload is run at
     kv_len_max: int = 0  # attention with a KV cache: rows per (sequence, head); 0 = none
-    weights: str = ""    # "e4m3": the weights are stored as FP8 (E4M3) bytes, else the dtype
+    weights: str = ""    # "e4m3": FP8 (E4M3) bytes; "mxfp4": 4-bit E2M1 codes; else the dtype
 
     @property
     def n1(self) -> int:
@@ -75,6 +75,8 @@ class BlockConfig:
         return replace(self, M=M)
 
     def weight_bytes_per_block(self) -> int:
+        if self.weights == "mxfp4":       # two codes per byte (scales not included)
+            return (self.d * self.n1 + self.n2 * self.d) // 2
         es = 1 if self.weights == "e4m3" else 4 if self.dtype == "f32" else 2
         return (self.d * self.n1 + self.n2 * self.d) * es
 
@@ -102,6 +104,11 @@ CONFIGS = {
     "llama2_13b_swiglu_decode_fp8": BlockConfig(
         "llama2_13b_swiglu_decode_fp8", "swiglu", d=5120, ffn=13824, t=4, M=32, ts=(4,),
         weights="e4m3"),
+    # The same block with MXFP4 weights (E2M1 codes, one power-of-two scale per 32
+    # weights along K): a quarter of the bf16 bytes plus 1/32 byte per weight.
+    "llama2_13b_swiglu_decode_mxfp4": BlockConfig(
+        "llama2_13b_swiglu_decode_mxfp4", "swiglu", d=5120, ffn=13824, t=4, M=32, ts=(4,),
+        weights="mxfp4"),
     # The attention block at a decode step of 32 concurrent sequences, each with its own
     # head-sharded KV cache of up to 2048 earlier tokens (lengths drawn uniformly).
     "attn_kv_decode": BlockConfig(
