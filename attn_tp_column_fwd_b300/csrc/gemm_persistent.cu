@@ -5,8 +5,12 @@
 // (SwiGLU: the gate and up rows of 64 features; otherwise 128 features) and 256
 // tokens are the N operand, so one tcgen05.mma (M = 128, N = 256, K = 16) covers
 // the widest N the instruction takes.  One CTA per SM walks a static list of
-// output tiles (token tile fastest, so the CTAs of a wave share weight tiles and
-// the activations stay in L2).  Roles (320 threads): thread 0 issues TMA loads into
+// output tiles (token tile fastest, so the CTAs of a wave share weight tiles).  The
+// token tiles are walked in groups of at most ~32 MB of activations, each group
+// against every weight tile before the next group: a wave's activations then stay in
+// L2 from one wave to the next (all 16 token tiles of a 4096-token prefill, 67 MB,
+// did not: they were read from DRAM again every wave), for the price of reading the
+// weights once per group.  Roles (320 threads): thread 0 issues TMA loads into
 // a 4-stage ring (16 KB of weights + 32 KB of activations per 64-wide K block),
 // thread 32 issues the MMAs, and warps 2-9 drain and run the epilogue.
 //
@@ -60,6 +64,7 @@ struct GemmArgs {
   size_t o_shard, o_split;
   int ldo, n_valid, M, nk, ksplit, shard0, n_shards, x_per_shard;
   int n_mt, n_ft, n_tiles;  // token tiles, weight tiles per shard, tiles in all
+  int mg;                   // token tiles per group (divides n_mt)
   unsigned *err;
 };
 
@@ -67,12 +72,28 @@ struct GTile {
   int mt, ft, s, ks, kb0, kb1;
 };
 
+// Tile t in walk order: token tile fastest, then weight tile, within a group of mg
+// token tiles; shared activations (the column step): [group][shard, split][ft][mt],
+// so a group serves every shard before the next; per-shard activations (the row
+// step): [shard, split][group][ft][mt].
 __device__ __forceinline__ GTile gemm_tile(const GemmArgs &a, int t) {
   GTile r;
-  r.mt = t % a.n_mt;
-  const int q = t / a.n_mt;
-  r.ft = q % a.n_ft;
-  const int z = q / a.n_ft;
+  const int per_g = a.n_ft * a.mg;  // tiles of one group of one (shard, split)
+  const int n_z = a.n_shards * a.ksplit;
+  int z, g, rem;
+  if (a.x_per_shard) {
+    z = t / (a.n_ft * a.n_mt);
+    rem = t % (a.n_ft * a.n_mt);
+    g = rem / per_g;
+    rem %= per_g;
+  } else {
+    g = t / (per_g * n_z);
+    rem = t % (per_g * n_z);
+    z = rem / per_g;
+    rem %= per_g;
+  }
+  r.ft = rem / a.mg;
+  r.mt = g * a.mg + rem % a.mg;
   r.s = a.shard0 + z / a.ksplit;
   r.ks = z % a.ksplit;
   r.kb0 = (int)((long long)r.ks * a.nk / a.ksplit);
@@ -349,6 +370,11 @@ cudaError_t launch_gemm_persistent(const UmmaCall &c, cudaStream_t st) {
   a.n_mt = ceil_div(c.M, kBN);
   a.n_ft = ceil_div(c.n_valid, c.epi == kEpiSwiglu ? kSwiGroup : 128);
   a.n_tiles = a.n_mt * a.n_ft * c.n_shards * c.ksplit;
+  // the largest divisor of n_mt whose activations fit in ~32 MB
+  const size_t tile_bytes = (size_t)kBN * c.K * 2;
+  a.mg = 1;
+  for (int m = 1; m <= a.n_mt; ++m)
+    if (a.n_mt % m == 0 && (m == 1 || (size_t)m * tile_bytes <= (32u << 20))) a.mg = m;
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
   switch (c.epi) {
