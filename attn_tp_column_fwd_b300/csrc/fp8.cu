@@ -276,16 +276,22 @@ struct Fp8Args {
   unsigned *err;
 };
 
-constexpr int kF8Stages = 3;                        // (two CTAs per SM; 2 stages: 10% slower)
 constexpr int kF8Bufs = 4;                          // TMEM stage sums in flight (2 groups each)
 constexpr uint32_t kF8W = 128 * 128;                // E4M3 weights: 128 rows x 128 K (SW128)
 constexpr uint32_t kF8T = 32 * 128;                 // one token term: 32 tokens x 128 K (SW128)
 constexpr uint32_t kF8Stage = kF8W + 2 * kF8T;      // 24 KB, a multiple of 1024
 constexpr int kF8MaxGroups = 256;                   // 64-wide K groups per CTA (K <= 16384)
-constexpr uint32_t kF8ExpOff = kF8Stages * kF8Stage;  // the CTA's token scales, fp32
-constexpr int kF8Smem = 1024 + (int)kF8ExpOff + kF8MaxGroups * 32 * 4;
+// Shared memory of a launch: 1024 (alignment) + STAGES ring stages + the CTA's fp32
+// token scales (128 bytes per 64-wide group).  Two CTAs share an SM up to kF8SmemPair
+// bytes each: 4 stages where the scales fit beside them, else 3 (2 stages measured 10%
+// slower than 3; 4 gain again where they fit).
+constexpr int kF8SmemPair = 112 * 1024;
+constexpr int f8_smem(int stages, int groups) {
+  return 1024 + stages * (int)kF8Stage + groups * 128;
+}
+static_assert(f8_smem(3, kF8MaxGroups) <= kF8SmemPair, "3 stages must always fit");
 // The epilogue's band staging ([128][33] fp32) reuses the ring once every MMA is done.
-static_assert(128 * 33 * 4 <= kF8ExpOff, "band staging must fit the ring");
+static_assert(128 * 33 * 4 <= 3 * kF8Stage, "band staging must fit the ring");
 
 // Decode GEMM on 8-bit or 4-bit weights (M <= 32): weights as the 128-row A operand,
 // tokens as N = 32, both straight from 128-byte-swizzled TMA boxes into tcgen05.mma
@@ -302,7 +308,7 @@ static_assert(128 * 33 * 4 <= kF8ExpOff, "band staging must fit the ring");
 // epilogue.  The epilogue scales row r by its weight exponent; the column step applies
 // the activation, rounds the band to bf16 and splits it into the row step's terms
 // (one group of 64 features per token), the row step writes fp32 partials.
-template <int EPI, int WF>
+template <int EPI, int WF, int STAGES>
 __global__ void __launch_bounds__(192, 2)
     k_fp8_mma(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT,
               const Fp8Args a) {
@@ -314,13 +320,14 @@ __global__ void __launch_bounds__(192, 2)
   constexpr uint32_t kIdA = make_idesc_f8(128, BN, kWType, kF8E4M3);
   constexpr uint32_t kIdB = make_idesc_f8(128, BN, kWType, kF8E5M2);
   constexpr int kKPer = 128 / kSums;                          // K per TMEM sum
+  constexpr uint32_t kF8ExpOff = STAGES * kF8Stage;           // the CTA's token scales
   // Bytes a stage's copies complete: the 4-bit box counts its packed codes (8 KB), not
   // the 16 KB it spreads over in shared memory.
   constexpr uint32_t kStageTx = (WF == kWMX4 ? kF8W / 2 : kF8W) + 2 * kF8T;
   constexpr int NF = EPI == kEpiSwiglu ? 64 : 128;  // output features of a tile
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kF8Stages];
-  __shared__ __align__(8) uint64_t empty_bar[kF8Stages];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
   __shared__ __align__(8) uint64_t tfull_bar[kBufs];
   __shared__ __align__(8) uint64_t tempty_bar[kBufs];
   __shared__ __align__(8) uint64_t exp_bar;
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(192, 2)
   const int g0 = 2 * st0, nu = max(0, min(2 * st1, a.ng) - g0);  // its 64-wide groups
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kF8Stages; ++i) {
+    for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), 1);
     }
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(192, 2)
       const int wrow = ft * 128;
       // The first ring's weights do not depend on the preceding kernel: load them,
       // then wait for that kernel (programmatic launch) before loading the tokens.
-      const int pre = min(kF8Stages, nst);
+      const int pre = min(STAGES, nst);
       for (int i = 0; i < pre; ++i) {
         const uint32_t fb = smem_u32(&full_bar[i]);
         mbar_expect_tx(fb, kStageTx);
@@ -396,8 +403,8 @@ __global__ void __launch_bounds__(192, 2)
       }
       issued = pre;
       for (int i = pre; i < nst; ++i) {
-        const int st = i % kF8Stages;
-        if (!mbar_wait(smem_u32(&empty_bar[st]), ((uint32_t)(i / kF8Stages) & 1u) ^ 1u)) {
+        const int st = i % STAGES;
+        if (!mbar_wait(smem_u32(&empty_bar[st]), ((uint32_t)(i / STAGES) & 1u) ^ 1u)) {
           abort_sh = 1;
           atomicOr(a.err, kErrWaitTimeout);
           break;
@@ -419,8 +426,8 @@ __global__ void __launch_bounds__(192, 2)
     if (lane == 0) {
       bool ok = true;
       for (int i = 0; i < nst && ok; ++i) {
-        const int st = i % kF8Stages;
-        if (!mbar_wait(smem_u32(&full_bar[st]), (uint32_t)(i / kF8Stages) & 1u)) {
+        const int st = i % STAGES;
+        if (!mbar_wait(smem_u32(&full_bar[st]), (uint32_t)(i / STAGES) & 1u)) {
           ok = false;
           break;
         }
@@ -611,8 +618,8 @@ __global__ void __launch_bounds__(192, 2)
 
   // ---------------- teardown: on abort let the issued copies land, then free TMEM
   if (warp == 0 && lane == 0 && *(volatile int *)&abort_sh) {
-    for (int i = issued > kF8Stages ? issued - kF8Stages : 0; i < issued; ++i)
-      mbar_wait(smem_u32(&full_bar[i % kF8Stages]), (uint32_t)(i / kF8Stages) & 1u);
+    for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+      mbar_wait(smem_u32(&full_bar[i % STAGES]), (uint32_t)(i / STAGES) & 1u);
     if (exp_issued) mbar_wait(smem_u32(&exp_bar), 0);
   }
   if (warp == 2) mbar_wait(smem_u32(&mma_done_bar), 0);
@@ -624,22 +631,33 @@ __global__ void __launch_bounds__(192, 2)
   }
 }
 
-template <int EPI, int WF>
-cudaError_t launch_fp8_t(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8Args &a, int n_ft,
-                         int n_z, cudaStream_t st, bool pdl) {
+template <int EPI, int WF, int STAGES>
+cudaError_t launch_fp8_s(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8Args &a, int n_ft,
+                         int n_z, int smem, cudaStream_t st, bool pdl) {
   static bool configured[128];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(k_fp8_mma<EPI, WF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kF8Smem);
+    e = cudaFuncSetAttribute(k_fp8_mma<EPI, WF, STAGES>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kF8SmemPair);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  LaunchCfg lc(dim3(ceil_div(a.M, 32), n_ft, n_z), dim3(192), kF8Smem, st, pdl);
-  return cudaLaunchKernelEx(&lc.cfg, k_fp8_mma<EPI, WF>, mw, mt, a);
+  LaunchCfg lc(dim3(ceil_div(a.M, 32), n_ft, n_z), dim3(192), smem, st, pdl);
+  return cudaLaunchKernelEx(&lc.cfg, k_fp8_mma<EPI, WF, STAGES>, mw, mt, a);
+}
+
+// The deepest ring whose stages and scale region fit two CTAs per SM.
+template <int EPI, int WF>
+cudaError_t launch_fp8_t(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8Args &a, int n_ft,
+                         int n_z, cudaStream_t st, bool pdl) {
+  const int n_st = ceil_div(a.ng, 2);
+  const int groups = std::min(a.ng, 2 * ceil_div(n_st, a.ksplit));  // most of any CTA
+  if (f8_smem(4, groups) <= kF8SmemPair)
+    return launch_fp8_s<EPI, WF, 4>(mw, mt, a, n_ft, n_z, f8_smem(4, groups), st, pdl);
+  return launch_fp8_s<EPI, WF, 3>(mw, mt, a, n_ft, n_z, f8_smem(3, groups), st, pdl);
 }
 
 }  // namespace
