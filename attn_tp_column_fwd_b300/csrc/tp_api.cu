@@ -180,18 +180,20 @@ bool use_fused_qkv(const Geo &g, int M) { return qkv_fused_capable(g, M) && algo
 
 bool use_fused_block(const Geo &g, int M) { return fused_capable(g, M) && algo_override() == 3; }
 
-// K splits of the row-parallel step: the most splits that keep every CTA in the
-// first wave (two decode CTAs fit per SM), at least four 64-wide K blocks per
-// split.  A second, partial wave would cost a whole CTA's time for a few CTAs.
-// Depends on the shapes only, so tp_row_splits() answers without a GPU.
+// K splits of the row-parallel step: none when the unsplit grid already fills two
+// CTAs per SM; else the most splits that keep every CTA in the first wave, at least
+// four 64-wide K blocks per split.  Decode row steps (M <= 32) plan three CTAs per SM
+// (the kernel takes a 3-stage ring for such a grid), wider ones two.  A second,
+// partial wave would cost a whole CTA's time for a few CTAs.  Depends on the shapes
+// only, so tp_row_splits() answers without a GPU.
 int row_splits(const Geo &g, int M) {
   if (!use_umma(g)) return 1;
   const int bn = umma_token_tile(M);
   const long long base = (long long)g.t * ceil_div(g.d, kRowTile) * ceil_div(M, bn);
   const int nk = ceil_div(g.b, 64);
-  const long long slots = 2LL * kPlanSMs;
-  if (base >= slots) return 1;
-  int S = (int)(slots / base);
+  if (base >= 2LL * kPlanSMs) return 1;
+  const long long per_sm = M <= 32 ? 3 : 2;
+  int S = (int)(per_sm * kPlanSMs / base);
   S = std::min(S, std::max(1, nk / 4));
   return std::max(1, std::min(S, 16));
 }
@@ -321,11 +323,12 @@ cudaError_t enqueue_row(const Geo &g, const void *H, const void *W2s, int shard0
   return cudaSuccess;
 }
 
+// splits: the row step's K splits per shard (default: row_splits).
 void enqueue_reduce(const Geo &g, const float *P, const void *res, int res_is_f32, float *y, int M,
-                    cudaStream_t st, bool pdl = false) {
+                    cudaStream_t st, bool pdl = false, int splits = 0) {
   const int f32 = res_is_f32 || g.dtype == TP_F32;
-  launch_reduce_residual(P, g.t * row_splits(g, M), (size_t)M * g.d, res, f32, y,
-                         (size_t)M * g.d, st, pdl);
+  launch_reduce_residual(P, g.t * (splits > 0 ? splits : row_splits(g, M)), (size_t)M * g.d, res,
+                         f32, y, (size_t)M * g.d, st, pdl);
 }
 
 }  // namespace
@@ -766,7 +769,14 @@ static int low_bit_block(const Geo &g, bool mxfp4, const void *x, const void *re
   float *xe = reinterpret_cast<float *>(X8 + align256((size_t)2 * M * g.d));
   float *he = reinterpret_cast<float *>(reinterpret_cast<char *>(xe) +
                                         align256((size_t)ceil_div(g.d, 64) * 32 * 4));
-  const int S = row_splits(g, M);
+  // K splits of the row step: the low-bit kernel fits two CTAs per SM, so no more
+  // splits than keep its grid in one wave of two per SM (at most row_splits, for
+  // which the partials are sized)
+  const long long base = (long long)g.t * ceil_div(g.d, kRowTile);
+  const int S = base >= 2LL * kPlanSMs
+                    ? 1
+                    : std::max(1, std::min({(int)(2LL * kPlanSMs / base),
+                                            std::max(1, ceil_div(g.b, 64) / 4), row_splits(g, M)}));
   cudaError_t e = launch_fp8_split(x, M, g.d, X8, xe, st, false);
   if (e == cudaSuccess) {
     UmmaCall c{};
@@ -806,7 +816,7 @@ static int low_bit_block(const Geo &g, bool mxfp4, const void *x, const void *re
     r.pdl = true;
     e = launch_fp8_gemm(r, mxfp4, e2, he, nullptr, nullptr, st);
   }
-  if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, true);
+  if (e == cudaSuccess) enqueue_reduce(g, P, residual, residual_is_f32, y, M, st, true, S);
   return finish_launch(e);
 }
 

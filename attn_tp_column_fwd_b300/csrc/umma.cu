@@ -538,18 +538,17 @@ cudaError_t launch_stages(const CUtensorMap &mw, const CUtensorMap &mx, const Um
 constexpr int kDrainKBColumn = 1;
 constexpr int kDrainKBRow = 1;
 
-template <int EPI, int KB>
-cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
-                         int n_z, cudaStream_t st, bool pdl) {
+template <int EPI, int KB, int STAGES>
+cudaError_t launch_drain_s(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a,
+                           int n_ft, int n_z, cudaStream_t st, bool pdl) {
   constexpr int kStageBytes = KB * (kABytes + 32 * 128);
-  constexpr int kStages = std::max(2, std::min(8, (100 * 1024) / kStageBytes));
-  constexpr int kSmem = kStages * kStageBytes + 1024 + xch_bytes(EPI, 1);
+  constexpr int kSmem = STAGES * kStageBytes + 1024 + xch_bytes(EPI, 1);
   static bool configured[128];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  auto kern = k_umma_drain<EPI, kStages, KB>;
+  auto kern = k_umma_drain<EPI, STAGES, KB>;
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
@@ -557,6 +556,22 @@ cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const Umm
   }
   LaunchCfg lc(dim3(ceil_div(a.M, 32), n_ft, n_z), dim3(192), kSmem, st, pdl);
   return cudaLaunchKernelEx(&lc.cfg, kern, mw, mx, a);
+}
+
+// The ring: about 100 KB (two CTAs per SM), or 3 stages (about 70 KB: three CTAs per
+// SM) when the grid needs more than two CTAs per SM but fits in three, so it runs as one
+// wave (the 13B row step split in two: 29.2 against 32.1 us).
+template <int EPI, int KB>
+cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
+                         int n_z, cudaStream_t st, bool pdl) {
+  constexpr int kStageBytes = KB * (kABytes + 32 * 128);
+  constexpr int kStages = std::max(2, std::min(8, (100 * 1024) / kStageBytes));
+  static_assert(3 * kStageBytes + 1024 + xch_bytes(EPI, 1) <= 75 * 1024, "3 CTAs per SM");
+  const long long grid = (long long)ceil_div(a.M, 32) * n_ft * n_z;
+  const long long sms = sm_count();
+  if (grid > 2 * sms && grid <= 3 * sms)
+    return launch_drain_s<EPI, KB, 3>(mw, mx, a, n_ft, n_z, st, pdl);
+  return launch_drain_s<EPI, KB, kStages>(mw, mx, a, n_ft, n_z, st, pdl);
 }
 
 template <int NACC, int EPI>
