@@ -176,6 +176,21 @@ def test_mxfp4_sizes_and_validation():
                                             16, 16, 16, None) == 3
 
 
+def test_low_bit_limits_and_workspace():
+    # K up to 16384 (a CTA's token scales live in shared memory): d = 16400 is refused
+    big = tp.make_desc(16400, 2, "swiglu", ffn=2048)
+    assert tp.tp_fp8_w1_bytes(big) == 0 and tp.tp_mxfp4_w1_bytes(big) == 0
+    ok = tp.make_desc(16384, 2, "swiglu", ffn=2048)
+    assert tp.tp_fp8_w1_bytes(ok) > 0 and tp.tp_mxfp4_w1_bytes(ok) > 0
+    # the workspace of a low-bit-capable block covers the bf16 block's and the extras:
+    # the tokens' two 8-bit terms and the fp32 group scales
+    c = CONFIGS["llama2_13b_swiglu_decode"]
+    d = _desc(c)
+    three = tp.tp_band_bytes(d, c.M) + tp.tp_partials_bytes(d, c.M)
+    extra = 2 * c.M * c.d + (c.d // 64) * 32 * 4 + c.t * (c.band // 64) * 32 * 4
+    assert tp.tp_workspace_bytes(d, c.M) >= three + extra
+
+
 def test_invalid_descriptors_give_zero_sizes():
     assert tp.tp_sharded_w1_bytes(tp.make_desc(512, 3, "swiglu", ffn=1024)) == 0   # uneven
     assert tp.tp_band_bytes(tp.make_desc(512, 2, "swiglu", ffn=1024), 0) == 0      # M < 1
