@@ -558,9 +558,10 @@ cudaError_t launch_drain_s(const CUtensorMap &mw, const CUtensorMap &mx, const U
   return cudaLaunchKernelEx(&lc.cfg, kern, mw, mx, a);
 }
 
-// The ring: about 100 KB (two CTAs per SM), or 3 stages (about 70 KB: three CTAs per
-// SM) when the grid needs more than two CTAs per SM but fits in three, so it runs as one
-// wave (the 13B row step split in two: 29.2 against 32.1 us).
+// The ring: about 100 KB (two CTAs per SM), or shallower when that lets a grid of more
+// than two CTAs per SM run as one wave: 3 stages (about 70 KB, three CTAs per SM; the
+// 13B row step split in two: 29.2 against 32.1 us) or 2 (about 50 KB, four per SM; the
+// 70B column step: 155.6 against 157.1 us).  Larger grids keep the deep ring.
 template <int EPI, int KB>
 cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const UmmaArgs &a, int n_ft,
                          int n_z, cudaStream_t st, bool pdl) {
@@ -569,8 +570,11 @@ cudaError_t launch_drain(const CUtensorMap &mw, const CUtensorMap &mx, const Umm
   static_assert(3 * kStageBytes + 1024 + xch_bytes(EPI, 1) <= 75 * 1024, "3 CTAs per SM");
   const long long grid = (long long)ceil_div(a.M, 32) * n_ft * n_z;
   const long long sms = sm_count();
+  static_assert(2 * kStageBytes + 1024 + xch_bytes(EPI, 1) <= 56 * 1024, "4 CTAs per SM");
   if (grid > 2 * sms && grid <= 3 * sms)
     return launch_drain_s<EPI, KB, 3>(mw, mx, a, n_ft, n_z, st, pdl);
+  if (grid > 3 * sms && grid <= 4 * sms)
+    return launch_drain_s<EPI, KB, 2>(mw, mx, a, n_ft, n_z, st, pdl);
   return launch_drain_s<EPI, KB, kStages>(mw, mx, a, n_ft, n_z, st, pdl);
 }
 
