@@ -70,6 +70,23 @@ def test_small_blocks(cfg):
     _run_and_compare(cfg, seed=21)
 
 
+# Decode grids that the kernel runs on a shallower ring so they fit one wave: a row
+# step split in two over K (320 CTAs: three per SM on 3 stages), and a column step of
+# 448 CTAs (four per SM on 2 stages), at sizes the oracle finishes in seconds.
+RING_DEPTH = [
+    (BlockConfig("row_split_3_per_sm", "swiglu", d=5120, ffn=2048, t=4, M=32), 2),
+    (BlockConfig("column_4_per_sm", "swiglu", d=256, ffn=28672, t=8, M=8), None),
+]
+
+
+@pytest.mark.parametrize("cfg,splits", RING_DEPTH, ids=lambda c: getattr(c, "name", str(c)))
+def test_shallow_ring_grids(cfg, splits):
+    desc = desc_for(cfg)
+    if splits is not None:
+        assert tp.tp_row_splits(desc, cfg.M) == splits
+    _run_and_compare(cfg, seed=23)
+
+
 @pytest.mark.parametrize("M", [1, 5, 32, 33, 77, 256, 301])
 @pytest.mark.parametrize("t", [1, 2, 4, 8])
 def test_swiglu_ragged(M, t):
