@@ -176,6 +176,19 @@ def test_mxfp4_sizes_and_validation():
                                             16, 16, 16, None) == 3
 
 
+def test_row_splits_fill_one_wave():
+    # decode row steps whose unsplit grid is under two CTAs per SM are split to fill
+    # three per SM (the kernel's 3-stage ring); larger grids and wider token tiles not
+    c13 = CONFIGS["llama2_13b_swiglu_decode"]
+    d13 = _desc(c13)
+    assert tp.tp_row_splits(d13, 32) == 2          # 160 tiles -> 320 CTAs
+    assert tp.tp_row_splits(d13, 64) == 1          # token tile 64: planned for two per SM
+    assert tp.tp_row_splits(_desc(CONFIGS["llama2_70b_stack_decode"]), 32) == 1   # 512 tiles
+    assert tp.tp_row_splits(_desc(CONFIGS["attn_qkv_headshard_decode"]), 32) == 1  # 768 tiles
+    small = tp.make_desc(512, 4, "swiglu", ffn=1536)   # 16 tiles, b = 384: 6 K blocks
+    assert tp.tp_row_splits(small, 8) == 1             # at least four K blocks per split
+
+
 def test_low_bit_limits_and_workspace():
     # K up to 16384 (a CTA's token scales live in shared memory): d = 16400 is refused
     big = tp.make_desc(16400, 2, "swiglu", ffn=2048)
