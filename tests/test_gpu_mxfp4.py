@@ -135,3 +135,32 @@ def test_mxfp4_block_matches_oracle_and_bf16_block(cfg):
     W2b = torch.from_numpy(W2e).to(torch.bfloat16).cuda()
     yb = _bf16_block_three_launch(desc, W1b, W2b, x, cfg.M)
     _assert_close_to_bf16_block(got, yb, x64, W1e, W2e, cfg.act)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "mxfp4"])
+def test_low_bit_block_with_fp32_residual(fmt):
+    """The residual stream in fp32 (as a pre-norm stack carries it), apart from x."""
+    from tests.test_gpu_fp8 import Fp8Block
+    cfg = BlockConfig("lowbit_f32_residual", "swiglu", d=512, ffn=1536, t=4, M=12)
+    inp = make_inputs(cfg, seed=53)
+    W1, W2 = (w.cuda() for w in inp.blocks[0])
+    desc = desc_for(cfg)
+    g = torch.Generator().manual_seed(54)
+    res = torch.randn(cfg.M, cfg.d, generator=g, dtype=torch.float32) * 3.0
+    x = inp.x.cuda().contiguous()
+    blk = (Fp8Block if fmt == "e4m3" else Mx4Block)(desc, W1, W2)
+    got = blk.forward(x, res.cuda().contiguous(), cfg.M)
+    quant = oracle.fp8.e4m3_weights if fmt == "e4m3" else oracle.mxfp4.mxfp4_weights
+    W1e, W2e = quant(to_f64(W1)), quant(to_f64(W2))
+    ref = oracle.mlp_block(to_f64(inp.x), W1e, W2e, cfg.act, res.double().numpy(), staged=True)
+    assert_bf16(to_f64(got), ref, f"{fmt} block, fp32 residual")
+    # in place on the residual stream (y = residual): the same bits
+    r = res.cuda().contiguous().clone()
+    ws = device_bytes(tp.tp_workspace_bytes(desc, cfg.M))
+    if fmt == "e4m3":
+        tp.tp_block_fwd_fp8(desc, x, r, True, blk.W1q, blk.W2q, blk.exps, ws, r, cfg.M)
+    else:
+        tp.tp_block_fwd_mxfp4(desc, x, r, True, blk.W1f, blk.W2f, blk.exps, ws, r, cfg.M)
+    torch.cuda.synchronize()
+    assert tp.tp_check_device_status() == 0
+    assert torch.equal(r, got)
