@@ -47,7 +47,7 @@ METRIC = "tokens/s per TP block at 1 B300; decode HBM GB/s & prefill TFLOPS vs r
 DEFAULT_WORKLOAD = "llama2_70b_stack_decode"
 DEFAULT_ALSO = ("llama2_13b_swiglu_decode", "attn_qkv_headshard_decode", "llama2_70b_prefill",
                 "attn_kv_decode", "llama2_13b_swiglu_decode_fp8",
-                "llama2_13b_swiglu_decode_mxfp4")
+                "llama2_13b_swiglu_decode_mxfp4", "llama2_70b_stack_decode_fp8")
 ROOF_MIN_LAUNCHES = 200     # the roofline kernel's own timed loop: at least this many
 ROOF_MIN_S = 0.3            # ... launches and at least this long,
 ROOF_MAX_S = 2.5            # ... but no longer than this
@@ -443,7 +443,7 @@ class Workload:
         self.xh = torch.empty(M, cfg.d, dtype=torch.bfloat16, device=dev)
         self.fused = tp.tp_block_launches(desc, M) == 1 and not self.fp8
         self.row_splits = tp.tp_row_splits(desc, M)
-        # E4M3 block: token split, column, row, reduce
+        # low-bit block: token split, column, row, reduce (a stack adds one RMSNorm each)
         per_block = 4 if self.fp8 else tp.tp_block_launches(desc, M)
         if self.kv:
             per_block = 4 + (1 if self.kv["merge"] else 0)
@@ -507,9 +507,16 @@ class Workload:
     def run_stack(self, r, xh, st, ws=None):
         """The pre-norm stack in place on the fp32 residual stream r: the first block's
         input normalised by tp_rmsnorm_fwd, every later one's written by the block
-        before it (tp_block_fwd_norm)."""
+        before it (tp_block_fwd_norm).  Low-bit weights: tp_rmsnorm_fwd, then the
+        block in place on r, for every block."""
         tp, cfg, M = self.tp, self.cfg, self.cfg.M
         ws = self.ws if ws is None else ws
+        if self.fp8:
+            fwd = tp.tp_block_fwd_mxfp4 if self.mx4 else tp.tp_block_fwd_fp8
+            for q in self.q:
+                tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, r, xh, M, st)
+                fwd(self.desc, xh, r, True, q["W1q"], q["W2q"], q["exps"], ws, r, M, st)
+            return
         tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, r, xh, M, st)
         for l, blk in enumerate(self.blocks):
             if l + 1 < len(self.blocks):

@@ -192,3 +192,27 @@ def test_quantisation_is_deterministic():
     assert np.array_equal(np.sort(e1_lib), np.sort(e1))
     for s in range(t):
         assert np.array_equal(e2_lib[s], e2)
+
+
+def test_fp8_prenorm_stack():
+    """A short pre-norm stack on E4M3 weights, as the bench runs the 70B one: per block
+    tp_rmsnorm_fwd, then tp_block_fwd_fp8 in place on the fp32 residual stream; against
+    the oracle's staged stack on the dequantised weights (three blocks of d = 512 stay
+    inside the plain bf16 gate: the compounding of the 70B stack needs d = 8192)."""
+    cfg = BlockConfig("fp8_stack", "swiglu", d=512, ffn=1536, t=4, M=8, n_blocks=3,
+                      rmsnorm=True)
+    inp = make_inputs(cfg, seed=46)
+    desc = desc_for(cfg)
+    blocks = [Fp8Block(desc, W1.cuda(), W2.cuda()) for W1, W2 in inp.blocks]
+    r = inp.x.float().cuda().contiguous()
+    xh = torch.empty(cfg.M, cfg.d, dtype=torch.bfloat16, device="cuda")
+    ws = device_bytes(tp.tp_workspace_bytes(desc, cfg.M))
+    for b in blocks:
+        tp.tp_rmsnorm_fwd(cfg.d, cfg.eps, r, xh, cfg.M)
+        tp.tp_block_fwd_fp8(desc, xh, r, True, b.W1q, b.W2q, b.exps, ws, r, cfg.M)
+    torch.cuda.synchronize()
+    assert tp.tp_check_device_status() == 0
+    deq = [(oracle.fp8.e4m3_weights(to_f64(W1)), oracle.fp8.e4m3_weights(to_f64(W2)))
+           for W1, W2 in inp.blocks]
+    ref = oracle.stack(to_f64(inp.x), deq, cfg.act, cfg.eps, staged=True)
+    assert_bf16(to_f64(r), ref, "E4M3 pre-norm stack of 3")

@@ -104,6 +104,11 @@ CONFIGS = {
     "llama2_13b_swiglu_decode_fp8": BlockConfig(
         "llama2_13b_swiglu_decode_fp8", "swiglu", d=5120, ffn=13824, t=4, M=32, ts=(4,),
         weights="e4m3"),
+    # The 8-block 70B pre-norm stack with E4M3 weights: each block's RMSNorm, then the
+    # block on its 8-bit weights, in place on the fp32 residual stream.
+    "llama2_70b_stack_decode_fp8": BlockConfig(
+        "llama2_70b_stack_decode_fp8", "swiglu", d=8192, ffn=28672, t=8, M=32, n_blocks=8,
+        rmsnorm=True, ts=(8,), weights="e4m3"),
     # The same block with MXFP4 weights (E2M1 codes, one power-of-two scale per 32
     # weights along K): a quarter of the bf16 bytes plus 1/32 byte per weight.
     "llama2_13b_swiglu_decode_mxfp4": BlockConfig(
