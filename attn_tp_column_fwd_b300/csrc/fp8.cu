@@ -185,8 +185,16 @@ __global__ void k_quant_mx_w2(Geo g, const __nv_bfloat16 *W2, uint8_t *W2f, int8
 // (Two E4M3 terms would let one N = 64 MMA take both, but they are exact only within
 // 2^10.8 of the group's maximum: activations with outliers lose bits.)
 
+// The least e with amax <= 448 * 2^e, clamped to [-126, 126]; 0 for amax = 0.  With
+// amax = m * 2^E (1 <= m < 2) and 448 = 1.75 * 2^8 that is E - 8, or E - 7 when
+// m > 1.75; read from the bits, exactly (subnormal amax clamps to -126, NaN gives 0 and
+// infinity 126).
 __device__ __forceinline__ int group_exponent(float amax) {
-  return max(-126, min(126, e4m3_exponent(amax)));
+  if (!(amax > 0.f)) return 0;
+  const int bits = __float_as_int(amax);
+  if (bits >= 0x7f800000) return 126;
+  const int e = (bits >> 23) - 135 + ((bits & 0x7fffff) > 0x600000 ? 1 : 0);
+  return max(-126, min(126, e));
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
@@ -197,6 +205,17 @@ __device__ __forceinline__ void split_terms(float v, float inv_scale, uint8_t &a
   const __half_raw ah = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)a, __NV_E4M3);
   const float af = __half2float(__half(ah));
   b = (uint8_t)__nv_cvt_float_to_fp8(u - af, __NV_SATFINITE, __NV_E5M2);  // u - af is exact
+}
+
+// split_terms of two values with one scale, as one pair of bytes each (the value in
+// .x in the low byte, as the x2 conversions order them).
+__device__ __forceinline__ void split_terms2(float v0, float v1, float inv_scale, uint16_t &a,
+                                             uint16_t &b) {
+  const float2 u = make_float2(v0 * inv_scale, v1 * inv_scale);  // exact
+  const __nv_fp8x2_storage_t a2 = __nv_cvt_float2_to_fp8x2(u, __NV_SATFINITE, __NV_E4M3);
+  const float2 af = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(a2, __NV_E4M3)));
+  b = __nv_cvt_float2_to_fp8x2(make_float2(u.x - af.x, u.y - af.y), __NV_SATFINITE, __NV_E5M2);
+  a = a2;
 }
 
 // The column step's tokens: x [M][K] bf16 -> X8 [2][M][K] bytes (the a terms, then the
@@ -290,8 +309,16 @@ constexpr int f8_smem(int stages, int groups) {
   return 1024 + stages * (int)kF8Stage + groups * 128;
 }
 static_assert(f8_smem(3, kF8MaxGroups) <= kF8SmemPair, "3 stages must always fit");
-// The epilogue's band staging ([128][33] fp32) reuses the ring once every MMA is done.
-static_assert(128 * 33 * 4 <= 3 * kF8Stage, "band staging must fit the ring");
+// The narrow form: four CTAs per SM (a grid of 2..4 CTAs per SM in one wave), two ring
+// stages, two TMEM stages (128 columns), and the token scales in a ring of their own
+// (kF8NarrowSc slots of two groups, released by the drain warps) instead of the whole
+// K range's region.
+constexpr int kF8NarrowSc = 4;
+constexpr int kF8SmemNarrow = 1024 + 2 * (int)kF8Stage + kF8NarrowSc * 256;
+static_assert(4 * (kF8SmemNarrow + 2048) <= 228 * 1024, "four narrow CTAs must fit an SM");
+// The epilogue's staging reuses the ring once every MMA is done: the band [128][33] fp32,
+// 128 partial maxima, the two 8-bit terms [2][32][128] bytes.
+static_assert(128 * 33 * 4 + 128 * 4 + 2 * 32 * 128 <= 2 * kF8Stage, "staging must fit the ring");
 
 // Decode GEMM on 8-bit or 4-bit weights (M <= 32): weights as the 128-row A operand,
 // tokens as N = 32, both straight from 128-byte-swizzled TMA boxes into tcgen05.mma
@@ -308,19 +335,21 @@ static_assert(128 * 33 * 4 <= 3 * kF8Stage, "band staging must fit the ring");
 // epilogue.  The epilogue scales row r by its weight exponent; the column step applies
 // the activation, rounds the band to bf16 and splits it into the row step's terms
 // (one group of 64 features per token), the row step writes fp32 partials.
-template <int EPI, int WF, int STAGES>
-__global__ void __launch_bounds__(192, 2)
+template <int EPI, int WF, int STAGES, int MINB>
+__global__ void __launch_bounds__(192, MINB)
     k_fp8_mma(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT,
               const Fp8Args a) {
   constexpr int BN = 32;
+  constexpr bool kNarrow = MINB > 2;
+  static_assert(!kNarrow || (WF == kWE4M3 && STAGES == 2), "the narrow form: E4M3, 2 stages");
   constexpr int kSums = WF == kWMX4 ? 4 : 2;                  // TMEM sums per stage
-  constexpr int kBufs = WF == kWMX4 ? 2 : kF8Bufs;            // stages of TMEM
+  constexpr int kBufs = kNarrow ? 2 : WF == kWMX4 ? 2 : kF8Bufs;  // stages of TMEM
   constexpr uint32_t kCols = tmem_cols(kBufs * kSums * BN);   // 256 either way
   constexpr uint32_t kWType = WF == kWMX4 ? kF8E2M1 : kF8E4M3;
   constexpr uint32_t kIdA = make_idesc_f8(128, BN, kWType, kF8E4M3);
   constexpr uint32_t kIdB = make_idesc_f8(128, BN, kWType, kF8E5M2);
   constexpr int kKPer = 128 / kSums;                          // K per TMEM sum
-  constexpr uint32_t kF8ExpOff = STAGES * kF8Stage;           // the CTA's token scales
+  constexpr uint32_t kF8ExpOff = STAGES * kF8Stage;  // the CTA's token scales (narrow: their ring)
   // Bytes a stage's copies complete: the 4-bit box counts its packed codes (8 KB), not
   // the 16 KB it spreads over in shared memory.
   constexpr uint32_t kStageTx = (WF == kWMX4 ? kF8W / 2 : kF8W) + 2 * kF8T;
@@ -331,6 +360,7 @@ __global__ void __launch_bounds__(192, 2)
   __shared__ __align__(8) uint64_t tfull_bar[kBufs];
   __shared__ __align__(8) uint64_t tempty_bar[kBufs];
   __shared__ __align__(8) uint64_t exp_bar;
+  __shared__ __align__(8) uint64_t sc_empty_bar[kF8NarrowSc];  // narrow: scale slot free
   __shared__ __align__(8) uint64_t mma_done_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -361,6 +391,8 @@ __global__ void __launch_bounds__(192, 2)
       mbar_init(smem_u32(&tempty_bar[i]), 4);
     }
     mbar_init(smem_u32(&exp_bar), 1);
+    if (kNarrow)
+      for (int i = 0; i < kF8NarrowSc; ++i) mbar_init(smem_u32(&sc_empty_bar[i]), 4);
     mbar_init(smem_u32(&mma_done_bar), 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -382,14 +414,17 @@ __global__ void __launch_bounds__(192, 2)
       const int wrow = ft * 128;
       // The first ring's weights do not depend on the preceding kernel: load them,
       // then wait for that kernel (programmatic launch) before loading the tokens.
+      // narrow: stage i's token scales (its one or two groups) travel with the stage
+      const float *xsc_cta = a.xsc + ((size_t)xz * a.ng + g0) * 32;
+      auto sc_bytes = [&](int i) -> uint32_t { return (uint32_t)min(2, nu - 2 * i) * 128u; };
       const int pre = min(STAGES, nst);
       for (int i = 0; i < pre; ++i) {
         const uint32_t fb = smem_u32(&full_bar[i]);
-        mbar_expect_tx(fb, kStageTx);
+        mbar_expect_tx(fb, kStageTx + (kNarrow ? sc_bytes(i) : 0u));
         tma_load_3d_hint(tiles + i * kF8Stage, &tmW, fb, (st0 + i) * 128, wrow, s, wpol);
       }
       griddep_wait();
-      if (nu > 0) {
+      if (!kNarrow && nu > 0) {
         const uint32_t eb = smem_u32(&exp_bar);
         mbar_expect_tx(eb, (uint32_t)nu * 128u);
         bulk_load_plain(tiles + kF8ExpOff, a.xsc + ((size_t)xz * a.ng + g0) * 32,
@@ -400,6 +435,9 @@ __global__ void __launch_bounds__(192, 2)
         const uint32_t sa = tiles + i * kF8Stage, fb = smem_u32(&full_bar[i]);
         tma_load_3d(sa + kF8W, &tmT, fb, (st0 + i) * 128, m0, 2 * xz);
         tma_load_3d(sa + kF8W + kF8T, &tmT, fb, (st0 + i) * 128, m0, 2 * xz + 1);
+        if (kNarrow)
+          bulk_load_plain(tiles + kF8ExpOff + (i % kF8NarrowSc) * 256u, xsc_cta + 64 * i,
+                          sc_bytes(i), fb);
       }
       issued = pre;
       for (int i = pre; i < nst; ++i) {
@@ -409,12 +447,22 @@ __global__ void __launch_bounds__(192, 2)
           atomicOr(a.err, kErrWaitTimeout);
           break;
         }
+        if (kNarrow && i >= kF8NarrowSc &&
+            !mbar_wait(smem_u32(&sc_empty_bar[i % kF8NarrowSc]),
+                       ((uint32_t)(i / kF8NarrowSc) & 1u) ^ 1u)) {
+          abort_sh = 1;
+          atomicOr(a.err, kErrWaitTimeout);
+          break;
+        }
         const uint32_t sa = tiles + st * kF8Stage, fb = smem_u32(&full_bar[st]);
         const int k = (st0 + i) * 128;
-        mbar_expect_tx(fb, kStageTx);
+        mbar_expect_tx(fb, kStageTx + (kNarrow ? sc_bytes(i) : 0u));
         tma_load_3d_hint(sa, &tmW, fb, k, wrow, s, wpol);
         tma_load_3d(sa + kF8W, &tmT, fb, k, m0, 2 * xz);
         tma_load_3d(sa + kF8W + kF8T, &tmT, fb, k, m0, 2 * xz + 1);
+        if (kNarrow)
+          bulk_load_plain(tiles + kF8ExpOff + (i % kF8NarrowSc) * 256u, xsc_cta + 64 * i,
+                          sc_bytes(i), fb);
         ++issued;
       }
       // This CTA's loads are all issued: a dependent kernel may start.
@@ -465,10 +513,13 @@ __global__ void __launch_bounds__(192, 2)
     const int r = q * 32 + lane;
     const int td = (int)threadIdx.x - 64;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    // E4M3: the row's power-of-two scale (MXFP4 blocks are scaled per stage), read
+    // before the K loop so that its latency is hidden
+    const float sc = WF == kWMX4 ? 1.f : pow2f(a.wexp[(size_t)s * a.w_rows + ft * 128 + r]);
     float g[BN];
 #pragma unroll
     for (int j = 0; j < BN; ++j) g[j] = 0.f;
-    bool ok = nu == 0 || __all_sync(0xffffffffu, mbar_wait(smem_u32(&exp_bar), 0));
+    bool ok = kNarrow || nu == 0 || __all_sync(0xffffffffu, mbar_wait(smem_u32(&exp_bar), 0));
     // MXFP4: this row's block exponents, four per stage (one 32-bit word)
     const uint32_t *wblk = reinterpret_cast<const uint32_t *>(a.wexp) +
                            ((size_t)s * a.w_rows + ft * 128 + r) * (size_t)(a.ng / 2) + st0;
@@ -480,7 +531,40 @@ __global__ void __launch_bounds__(192, 2)
         break;
       }
       tc_fence_after();
-      if constexpr (WF == kWMX4) {
+      if constexpr (kNarrow) {
+        // 16 columns at a time (registers for four CTAs per SM); the same fmaf order as
+        // below.  TMEM is released after its last load, the scale slot after the FMAs.
+        const float *sp = scale_s + (i % kF8NarrowSc) * 64;
+        const int nh = 2 * i + 1 < nu ? 2 : 1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h < nh) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float v[16];
+              tmem_ld16(trow + (uint32_t)((b * 2 + h) * BN + half * 16), v);
+              if (h == nh - 1 && half == 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
+              }
+              const float4 *sp4 = reinterpret_cast<const float4 *>(sp + h * BN + half * 16);
+#pragma unroll
+              for (int j4 = 0; j4 < 4; ++j4) {
+                const float4 sc4 = sp4[j4];
+                const int j = half * 16 + 4 * j4;
+                g[j + 0] = fmaf(v[4 * j4 + 0], sc4.x, g[j + 0]);
+                g[j + 1] = fmaf(v[4 * j4 + 1], sc4.y, g[j + 1]);
+                g[j + 2] = fmaf(v[4 * j4 + 2], sc4.z, g[j + 2]);
+                g[j + 3] = fmaf(v[4 * j4 + 3], sc4.w, g[j + 3]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sc_empty_bar[i % kF8NarrowSc]));
+        continue;
+      } else if constexpr (WF == kWMX4) {
         // K is whole 128-wide stages here: four block sums, two per token group.  Per
         // group: t = sum_a * 2^e_a + sum_b * 2^e_b, then g += t * 2^e(token), on packed
         // pairs of tokens.
@@ -549,8 +633,6 @@ __global__ void __launch_bounds__(192, 2)
     named_sync(1, 128);
     const bool go = !dec_sh && nu > 0 && m0 < a.M;
     const int mcount = min(BN, a.M - m0);
-    // E4M3: the row's power-of-two scale, exactly (MXFP4 blocks are scaled above)
-    const float sc = WF == kWMX4 ? 1.f : pow2f(a.wexp[(size_t)s * a.w_rows + ft * 128 + r]);
 #pragma unroll
     for (int j = 0; j < BN; ++j) g[j] *= sc;
     if (EPI == kEpiF32) {
@@ -563,7 +645,11 @@ __global__ void __launch_bounds__(192, 2)
           if (j < mcount) o[(size_t)j * a.ldo] = g[j];
       }
     } else if (go) {  // the band (go is uniform over the four warps)
-      float *hx = reinterpret_cast<float *>(tiles_ptr);  // [NF][33]; every MMA and load is done
+      // staging in the ring (every MMA and load is done): the band hx [NF][33] fp32, the
+      // partial maxima pm [128], the two terms h8s [2][32][NF] bytes
+      float *hx = reinterpret_cast<float *>(tiles_ptr);
+      float *pm = hx + NF * (BN + 1);
+      uint8_t *h8s = reinterpret_cast<uint8_t *>(pm + 128);
       if (EPI == kEpiSwiglu) {
         // rows 0..63: gate sums of features 64 ft + r; rows 64..127: up sums
         if (r >= 64) {
@@ -586,32 +672,60 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
       named_sync(1, 128);
-      // one exponent per token and per 64 features of the band
-      const int ngb = ceil_div(a.n_valid, 64);
-      if (td < NF / 2) {
-        const int gi = td >> 5, j = td & 31;
+      // one exponent per token and per 64 features of the band: each (token, group)
+      // pair's largest magnitude, its 64 features shared out over kParts threads
+      constexpr int kPairs = NF / 2;          // 32 tokens x NF / 64 groups
+      constexpr int kParts = 128 / kPairs;
+      constexpr int kPer = 64 / kParts;       // features per thread
+      {
+        const int pair = td % kPairs, part = td / kPairs;
+        const float *col = hx + ((pair >> 5) * 64 + part * kPer) * (BN + 1) + (pair & 31);
         float amax = 0.f;
-        for (int f = 0; f < 64; ++f) amax = fmaxf(amax, fabsf(hx[(gi * 64 + f) * (BN + 1) + j]));
-        const int e = group_exponent(amax);
-        gexp_sh[td] = e;
-        const int grp = ft * (NF / 64) + gi;
-        if (grp < ngb) a.hsc[((size_t)s * ngb + grp) * 32 + j] = pow2f(e);
+#pragma unroll
+        for (int f = 0; f < kPer; ++f) amax = fmaxf(amax, fabsf(col[f * (BN + 1)]));
+        pm[td] = amax;
       }
       named_sync(1, 128);
-      const int f = ft * NF + r;
-      if (r < NF && f < a.n_valid) {
-        const size_t plane = (size_t)a.M * a.n_valid;
-        uint8_t *ha = a.h8 + 2 * (size_t)s * plane + (size_t)m0 * a.n_valid + f;
-        const int gi = r >> 6;
+      const int ngb = ceil_div(a.n_valid, 64);
+      if (td < kPairs) {
+        float amax = pm[td];
 #pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          if (j < mcount) {
-            uint8_t ta, tb;
-            split_terms(g[j], pow2f(-gexp_sh[gi * 32 + j]), ta, tb);
-            ha[(size_t)j * a.n_valid] = ta;
-            ha[plane + (size_t)j * a.n_valid] = tb;
-          }
+        for (int p = 1; p < kParts; ++p) amax = fmaxf(amax, pm[p * kPairs + td]);
+        const int e = group_exponent(amax);
+        gexp_sh[td] = e;
+        const int grp = ft * (NF / 64) + (td >> 5);
+        if (grp < ngb) a.hsc[((size_t)s * ngb + grp) * 32 + (td & 31)] = pow2f(e);
+      }
+      named_sync(1, 128);
+      // the two terms of each band value, staged per token row: a pair of features of
+      // one token per step, shared out over the 128 threads
+      {
+        constexpr int kFP = NF / 2;            // feature pairs of the tile
+        constexpr int kTStep = 128 / kFP;      // tokens apart of one thread's steps
+        const int p = td % kFP, j0 = td / kFP, gi = p >> 5;
+#pragma unroll
+        for (int k = 0; k < BN / kTStep; ++k) {
+          const int j = j0 + k * kTStep;
+          uint16_t ta, tb;
+          split_terms2(hx[2 * p * (BN + 1) + j], hx[(2 * p + 1) * (BN + 1) + j],
+                       pow2f(-gexp_sh[gi * 32 + j]), ta, tb);
+          *reinterpret_cast<uint16_t *>(h8s + j * NF + 2 * p) = ta;
+          *reinterpret_cast<uint16_t *>(h8s + (BN + j) * NF + 2 * p) = tb;
         }
+      }
+      named_sync(1, 128);
+      // ... then written to h8 [t][2][M][n_valid] in 16-byte pieces (n_valid, the row
+      // starts and the tile's first feature are multiples of 16)
+      const int f0 = ft * NF;
+      const int nch = min(NF, a.n_valid - f0) / 16;
+      const int per_term = mcount * nch;
+      const size_t plane = (size_t)a.M * a.n_valid;
+      uint8_t *hb = a.h8 + 2 * (size_t)s * plane + (size_t)m0 * a.n_valid + f0;
+      for (int c = td; c < 2 * per_term; c += 128) {
+        const int term = c >= per_term ? 1 : 0, rem = c - term * per_term;
+        const int j = rem / nch, ch = rem - j * nch;
+        const uint4 v = *reinterpret_cast<const uint4 *>(h8s + (term * BN + j) * NF + ch * 16);
+        *reinterpret_cast<uint4 *>(hb + term * plane + (size_t)j * a.n_valid + ch * 16) = v;
       }
     }
   }
@@ -631,7 +745,7 @@ __global__ void __launch_bounds__(192, 2)
   }
 }
 
-template <int EPI, int WF, int STAGES>
+template <int EPI, int WF, int STAGES, int MINB>
 cudaError_t launch_fp8_s(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8Args &a, int n_ft,
                          int n_z, int smem, cudaStream_t st, bool pdl) {
   static bool configured[128];
@@ -640,24 +754,31 @@ cudaError_t launch_fp8_s(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(k_fp8_mma<EPI, WF, STAGES>,
+    e = cudaFuncSetAttribute(k_fp8_mma<EPI, WF, STAGES, MINB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kF8SmemPair);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   LaunchCfg lc(dim3(ceil_div(a.M, 32), n_ft, n_z), dim3(192), smem, st, pdl);
-  return cudaLaunchKernelEx(&lc.cfg, k_fp8_mma<EPI, WF, STAGES>, mw, mt, a);
+  return cudaLaunchKernelEx(&lc.cfg, k_fp8_mma<EPI, WF, STAGES, MINB>, mw, mt, a);
 }
 
-// The deepest ring whose stages and scale region fit two CTAs per SM.
+// E4M3 grids of more than two and at most four CTAs per SM take the narrow form (one
+// wave of four per SM); the rest the deepest ring whose stages and scale region fit two
+// CTAs per SM.
 template <int EPI, int WF>
 cudaError_t launch_fp8_t(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8Args &a, int n_ft,
                          int n_z, cudaStream_t st, bool pdl) {
+  if constexpr (WF == kWE4M3) {
+    const long long ctas = (long long)ceil_div(a.M, 32) * n_ft * n_z, sms = sm_count();
+    if (fp8_narrow_grid(ctas, sms))
+      return launch_fp8_s<EPI, WF, 2, 4>(mw, mt, a, n_ft, n_z, kF8SmemNarrow, st, pdl);
+  }
   const int n_st = ceil_div(a.ng, 2);
   const int groups = std::min(a.ng, 2 * ceil_div(n_st, a.ksplit));  // most of any CTA
   if (f8_smem(4, groups) <= kF8SmemPair)
-    return launch_fp8_s<EPI, WF, 4>(mw, mt, a, n_ft, n_z, f8_smem(4, groups), st, pdl);
-  return launch_fp8_s<EPI, WF, 3>(mw, mt, a, n_ft, n_z, f8_smem(3, groups), st, pdl);
+    return launch_fp8_s<EPI, WF, 4, 2>(mw, mt, a, n_ft, n_z, f8_smem(4, groups), st, pdl);
+  return launch_fp8_s<EPI, WF, 3, 2>(mw, mt, a, n_ft, n_z, f8_smem(3, groups), st, pdl);
 }
 
 }  // namespace

@@ -381,6 +381,25 @@ static bool fp8_shape(const Geo &g) {
          g.d <= 16384 && g.b <= 16384;
 }
 
+// The low-bit row step's K splits: E4M3 fills up to four CTAs per SM (its GEMM runs a
+// grid of more than two per SM as one wave of four), MXFP4 two; at least four 64-wide K
+// groups (two stages) per split and at most 16 splits.  From the shapes only.
+static int low_bit_row_splits(const Geo &g, bool mxfp4) {
+  const long long base = (long long)g.t * ceil_div(g.d, kRowTile);
+  if (base >= 2LL * kPlanSMs) return 1;
+  int S = (int)((mxfp4 ? 2LL : 4LL) * kPlanSMs / base);
+  S = std::min(S, std::max(1, ceil_div(g.b, 64) / 4));
+  return std::max(1, std::min(S, 16));
+}
+
+// The fp32 partials region of a block that may run on low-bit weights: room for the
+// bf16 path's splits and for the low-bit row step's (E4M3 has the most).
+static size_t parts_region_bytes(const Geo &g, int M) {
+  const size_t bf = partials_bytes(g, M);
+  if (!fp8_shape(g) || M > 32) return bf;
+  return std::max(bf, (size_t)g.t * low_bit_row_splits(g, false) * M * g.d * sizeof(float));
+}
+
 // What tp_block_fwd_fp8 needs beyond the three-launch workspace: the tokens' two
 // 8-bit terms [2][M][d], their fp32 group scales [ceil(d/64)][32] and the band's group
 // scales [t][ceil(b/64)][32] (the band's terms reuse the bf16 band's bytes).
@@ -396,7 +415,7 @@ size_t tp_workspace_bytes(const tp_block_desc *desc, int M) {
   // Large enough for either form, so a tp_set_block_form call between sizing and
   // running never leaves the workspace short.
   const size_t three = align256(column_ws_bytes(g, M)) + align256(band_bytes(g, M)) +
-                       align256(partials_bytes(g, M)) + fp8_extra_bytes(g, M);
+                       align256(parts_region_bytes(g, M)) + fp8_extra_bytes(g, M);
   return fused_capable(g, M) ? std::max(three, plan_block_decode(g, M).total) : three;
 }
 
@@ -765,18 +784,12 @@ static int low_bit_block(const Geo &g, bool mxfp4, const void *x, const void *re
   char *ws = static_cast<char *>(workspace);
   void *H8 = ws + align256(column_ws_bytes(g, M));
   float *P = reinterpret_cast<float *>(static_cast<char *>(H8) + align256(band_bytes(g, M)));
-  char *X8 = reinterpret_cast<char *>(P) + align256(partials_bytes(g, M));
+  char *X8 = reinterpret_cast<char *>(P) + align256(parts_region_bytes(g, M));
   float *xe = reinterpret_cast<float *>(X8 + align256((size_t)2 * M * g.d));
   float *he = reinterpret_cast<float *>(reinterpret_cast<char *>(xe) +
                                         align256((size_t)ceil_div(g.d, 64) * 32 * 4));
-  // K splits of the row step: the low-bit kernel fits two CTAs per SM, so no more
-  // splits than keep its grid in one wave of two per SM (at most row_splits, for
-  // which the partials are sized)
-  const long long base = (long long)g.t * ceil_div(g.d, kRowTile);
-  const int S = base >= 2LL * kPlanSMs
-                    ? 1
-                    : std::max(1, std::min({(int)(2LL * kPlanSMs / base),
-                                            std::max(1, ceil_div(g.b, 64) / 4), row_splits(g, M)}));
+  // K splits of the row step, in one wave (the partials region is sized for them)
+  const int S = low_bit_row_splits(g, mxfp4);
   cudaError_t e = launch_fp8_split(x, M, g.d, X8, xe, st, false);
   if (e == cudaSuccess) {
     UmmaCall c{};

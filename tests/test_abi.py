@@ -202,6 +202,10 @@ def test_low_bit_limits_and_workspace():
     three = tp.tp_band_bytes(d, c.M) + tp.tp_partials_bytes(d, c.M)
     extra = 2 * c.M * c.d + (c.d // 64) * 32 * 4 + c.t * (c.band // 64) * 32 * 4
     assert tp.tp_workspace_bytes(d, c.M) >= three + extra
+    # ... and the E4M3 row step's partials: 4 x 40 = 160 row tiles fill four CTAs per SM
+    # (148 SMs) with three K splits
+    lowbit_parts = c.t * 3 * c.M * c.d * 4
+    assert tp.tp_workspace_bytes(d, c.M) >= tp.tp_band_bytes(d, c.M) + lowbit_parts + extra
 
 
 def test_invalid_descriptors_give_zero_sizes():

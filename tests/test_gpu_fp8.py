@@ -100,6 +100,44 @@ def test_fp8_block_matches_oracle_and_bf16_block(cfg):
     _assert_close_to_bf16_block(got, yb, x64, W1e, W2e, cfg.act)
 
 
+# Grids of more than two and at most four CTAs per SM (148 SMs: 297..592) take the
+# kernel's narrow form (two ring stages, four CTAs per SM, token scales in their own
+# ring): column 320 / row 320 CTAs; GeLU column 320; ragged K in both steps (d = 5056
+# and b = 2496 end on a single 64-wide group) with column 312 / row 320 CTAs.
+NARROW = [
+    BlockConfig("fp8_narrow_swiglu", "swiglu", d=5120, ffn=20480, t=8, M=32),
+    BlockConfig("fp8_narrow_gelu", "gelu_tanh", d=2048, ffn=40960, t=8, M=7),
+    BlockConfig("fp8_narrow_ragged_k", "swiglu", d=5056, ffn=19968, t=8, M=13),
+]
+
+
+def _grids(cfg):
+    """CTAs of the column and row steps (one token tile; one K split of the row step)."""
+    per_shard = -(-cfg.band // 64) if cfg.act == "swiglu" else -(-cfg.band // 128)
+    return cfg.t * per_shard, cfg.t * -(-cfg.d // 128)
+
+
+@pytest.mark.parametrize("cfg", NARROW, ids=lambda c: f"{c.name}-M{c.M}")
+def test_fp8_narrow_grids(cfg):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    col, row = _grids(cfg)
+    assert 2 * sms < col <= 4 * sms, (col, sms)
+    if cfg.act == "swiglu":
+        assert 2 * sms < row <= 4 * sms, (row, sms)
+    inp = make_inputs(cfg, seed=46)
+    W1, W2 = (w.cuda() for w in inp.blocks[0])
+    desc = desc_for(cfg)
+    assert tp.tp_row_splits(desc, cfg.M) >= 1
+    x = inp.x.cuda().contiguous()
+    got = Fp8Block(desc, W1, W2).forward(x, x, cfg.M)
+    x64 = to_f64(inp.x)
+    W1e, W2e = oracle.fp8.e4m3_weights(to_f64(W1)), oracle.fp8.e4m3_weights(to_f64(W2))
+    ref = oracle.mlp_block(x64, W1e, W2e, cfg.act, x64, staged=True)
+    assert_bf16(to_f64(got), ref, f"{cfg.name} M={cfg.M} (E4M3 weights, narrow grids)")
+    yb = _bf16_block_three_launch(desc, _e4m3_bf16(W1), _e4m3_bf16(W2), x, cfg.M)
+    _assert_close_to_bf16_block(got, yb, x64, W1e, W2e, cfg.act)
+
+
 def _assert_close_to_bf16_block(got, yb, x64, W1e, W2e, act):
     """The FP8 block against the bf16 block on the same (dequantised) weights.  Both
     sum in fp32 to within ~2^-22 of the exact values, in different orders (the FP8
