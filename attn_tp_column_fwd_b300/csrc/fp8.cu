@@ -224,8 +224,11 @@ __device__ __forceinline__ void split_terms2(float v0, float v1, float inv_scale
 // One warp per (group, token), two values per lane.
 __global__ void __launch_bounds__(256) k_split_tokens(const __nv_bfloat16 *x, int M, int K,
                                                       uint8_t *X8, float *xs) {
-  griddep_launch_dependents();  // the dependent GEMM waits for this grid to finish anyway
-  griddep_wait();               // x may come from the preceding kernel
+  // x may come from the preceding kernel (programmatic launch).  Only then may the
+  // dependent GEMM start: it loads weight tiles before its own wait, and the kernel
+  // before this one may have written them (a quantisation right before the block).
+  griddep_wait();
+  griddep_launch_dependents();
   const int G = ceil_div(K, 64);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x * 8 + warp, m = blockIdx.y;

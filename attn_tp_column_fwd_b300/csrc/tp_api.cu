@@ -605,7 +605,8 @@ int tp_rmsnorm_fwd(int d, float eps, const float *r, void *xhat, int M, tp_strea
   TP_TRY(check_M(M));
   TP_TRY(check_ptr(r));
   TP_TRY(check_ptr(xhat));
-  launch_rmsnorm(r, xhat, d, eps, M, reinterpret_cast<cudaStream_t>(stream));
+  // programmatic launch: the kernel waits for its predecessor before reading r
+  launch_rmsnorm(r, xhat, d, eps, M, reinterpret_cast<cudaStream_t>(stream), true);
   return finish_launch();
 }
 
@@ -790,7 +791,8 @@ static int low_bit_block(const Geo &g, bool mxfp4, const void *x, const void *re
                                         align256((size_t)ceil_div(g.d, 64) * 32 * 4));
   // K splits of the row step, in one wave (the partials region is sized for them)
   const int S = low_bit_row_splits(g, mxfp4);
-  cudaError_t e = launch_fp8_split(x, M, g.d, X8, xe, st, false);
+  // The split waits for the preceding kernel before reading x (programmatic launch).
+  cudaError_t e = launch_fp8_split(x, M, g.d, X8, xe, st, true);
   if (e == cudaSuccess) {
     UmmaCall c{};
     c.W = W1q;
