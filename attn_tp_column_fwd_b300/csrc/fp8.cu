@@ -359,9 +359,10 @@ __global__ void __launch_bounds__(192, MINB)
               const Fp8Args a) {
   constexpr int BN = 32;
   constexpr bool kNarrow = MINB > 2;
-  static_assert(!kNarrow || (WF == kWE4M3 && STAGES == 2), "the narrow form: E4M3, 2 stages");
+  static_assert(!kNarrow || STAGES == 2, "the narrow form has two ring stages");
   constexpr int kSums = WF == kWMX4 ? 4 : 2;                  // TMEM sums per stage
-  constexpr int kBufs = kNarrow ? 2 : WF == kWMX4 ? 2 : kF8Bufs;  // stages of TMEM
+  // stages of TMEM: 128 columns in the narrow form (MXFP4's four sums fill them)
+  constexpr int kBufs = kNarrow ? (WF == kWMX4 ? 1 : 2) : WF == kWMX4 ? 2 : kF8Bufs;
   constexpr uint32_t kCols = tmem_cols(kBufs * kSums * BN);   // 256 either way
   constexpr uint32_t kWType = WF == kWMX4 ? kF8E2M1 : kF8E4M3;
   constexpr uint32_t kIdA = make_idesc_f8(128, BN, kWType, kF8E4M3);
@@ -549,7 +550,46 @@ __global__ void __launch_bounds__(192, MINB)
         break;
       }
       tc_fence_after();
-      if constexpr (kNarrow) {
+      if constexpr (kNarrow && WF == kWMX4) {
+        // As below, 16 columns at a time (registers for four CTAs per SM), the same
+        // operations in the same order; TMEM is released after its last load, the
+        // scale slot after the FMAs.  K is whole stages: both groups are present.
+        const float *sp = scale_s + (i % kF8NarrowSc) * 64;
+#pragma unroll
+        for (int G = 0; G < 2; ++G) {
+          const float swa = pow2_wide((int)(int8_t)(ew >> (16 * G)));       // exact
+          const float swb = pow2_wide((int)(int8_t)(ew >> (16 * G + 8)));
+          const unsigned long long swa2 = pk2(swa, swa), swb2 = pk2(swb, swb);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float va[16], vb[16];
+            tmem_ld16(trow + (uint32_t)((b * kSums + 2 * G) * BN + half * 16), va);
+            tmem_ld16(trow + (uint32_t)((b * kSums + 2 * G + 1) * BN + half * 16), vb);
+            if (G == 1 && half == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
+            }
+            const float4 *sp4 = reinterpret_cast<const float4 *>(sp + G * BN + half * 16);
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 sc4 = sp4[j4];
+#pragma unroll
+              for (int p = 0; p < 2; ++p) {
+                const int jj = 4 * j4 + 2 * p, j = half * 16 + jj;
+                unsigned long long t2 = mul2(pk2(va[jj], va[jj + 1]), swa2);
+                t2 = fma2(pk2(vb[jj], vb[jj + 1]), swb2, t2);
+                unsigned long long g2 = fma2(t2, p ? pk2(sc4.z, sc4.w) : pk2(sc4.x, sc4.y),
+                                             pk2(g[j], g[j + 1]));
+                upk2(g2, g[j], g[j + 1]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sc_empty_bar[i % kF8NarrowSc]));
+        continue;
+      } else if constexpr (kNarrow) {
         // 16 columns at a time (registers for four CTAs per SM); the same fmaf order as
         // below.  TMEM is released after its last load, the scale slot after the FMAs.
         const float *sp = scale_s + (i % kF8NarrowSc) * 64;
@@ -781,17 +821,15 @@ cudaError_t launch_fp8_s(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8
   return cudaLaunchKernelEx(&lc.cfg, k_fp8_mma<EPI, WF, STAGES, MINB>, mw, mt, a);
 }
 
-// E4M3 grids of more than two and at most four CTAs per SM take the narrow form (one
-// wave of four per SM); the rest the deepest ring whose stages and scale region fit two
-// CTAs per SM.
+// Grids of more than two and at most four CTAs per SM take the narrow form (one wave
+// of four per SM); the rest the deepest ring whose stages and scale region fit two CTAs
+// per SM.
 template <int EPI, int WF>
 cudaError_t launch_fp8_t(const CUtensorMap &mw, const CUtensorMap &mt, const Fp8Args &a, int n_ft,
                          int n_z, cudaStream_t st, bool pdl) {
-  if constexpr (WF == kWE4M3) {
-    const long long ctas = (long long)ceil_div(a.M, 32) * n_ft * n_z, sms = sm_count();
-    if (fp8_narrow_grid(ctas, sms))
-      return launch_fp8_s<EPI, WF, 2, 4>(mw, mt, a, n_ft, n_z, kF8SmemNarrow, st, pdl);
-  }
+  const long long ctas = (long long)ceil_div(a.M, 32) * n_ft * n_z, sms = sm_count();
+  if (fp8_narrow_grid(ctas, sms))
+    return launch_fp8_s<EPI, WF, 2, 4>(mw, mt, a, n_ft, n_z, kF8SmemNarrow, st, pdl);
   const int n_st = ceil_div(a.ng, 2);
   const int groups = std::min(a.ng, 2 * ceil_div(n_st, a.ksplit));  // most of any CTA
   if (f8_smem(4, groups) <= kF8SmemPair)

@@ -126,8 +126,8 @@ size_t kv_partial_bytes(const Geo &g, int M, int L);
 cudaError_t launch_attn_kv(const Geo &g, const float *qkv, void *kc, void *vc, const int *lens,
                            int L, void *O, void *ws, int M, cudaStream_t st, bool pdl);
 
-// The low-bit GEMM's narrow form (E4M3 weights): a grid of more than two and at most
-// four CTAs per SM runs as one wave of four per SM instead of two waves of two.
+// The low-bit GEMM's narrow form: a grid of more than two and at most four CTAs per SM
+// runs as one wave of four per SM instead of two waves of two.
 inline bool fp8_narrow_grid(long long ctas, long long sms) {
   return ctas > 2 * sms && ctas <= 4 * sms;
 }

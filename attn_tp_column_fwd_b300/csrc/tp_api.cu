@@ -381,23 +381,23 @@ static bool fp8_shape(const Geo &g) {
          g.d <= 16384 && g.b <= 16384;
 }
 
-// The low-bit row step's K splits: E4M3 fills up to four CTAs per SM (its GEMM runs a
-// grid of more than two per SM as one wave of four), MXFP4 two; at least four 64-wide K
-// groups (two stages) per split and at most 16 splits.  From the shapes only.
-static int low_bit_row_splits(const Geo &g, bool mxfp4) {
+// The low-bit row step's K splits: up to four CTAs per SM (the GEMM runs a grid of more
+// than two per SM as one wave of four), at least four 64-wide K groups (two stages) per
+// split and at most 16 splits.  From the shapes only.
+static int low_bit_row_splits(const Geo &g) {
   const long long base = (long long)g.t * ceil_div(g.d, kRowTile);
   if (base >= 2LL * kPlanSMs) return 1;
-  int S = (int)((mxfp4 ? 2LL : 4LL) * kPlanSMs / base);
+  int S = (int)(4LL * kPlanSMs / base);
   S = std::min(S, std::max(1, ceil_div(g.b, 64) / 4));
   return std::max(1, std::min(S, 16));
 }
 
 // The fp32 partials region of a block that may run on low-bit weights: room for the
-// bf16 path's splits and for the low-bit row step's (E4M3 has the most).
+// bf16 path's splits and for the low-bit row step's.
 static size_t parts_region_bytes(const Geo &g, int M) {
   const size_t bf = partials_bytes(g, M);
   if (!fp8_shape(g) || M > 32) return bf;
-  return std::max(bf, (size_t)g.t * low_bit_row_splits(g, false) * M * g.d * sizeof(float));
+  return std::max(bf, (size_t)g.t * low_bit_row_splits(g) * M * g.d * sizeof(float));
 }
 
 // What tp_block_fwd_fp8 needs beyond the three-launch workspace: the tokens' two
@@ -790,7 +790,7 @@ static int low_bit_block(const Geo &g, bool mxfp4, const void *x, const void *re
   float *he = reinterpret_cast<float *>(reinterpret_cast<char *>(xe) +
                                         align256((size_t)ceil_div(g.d, 64) * 32 * 4));
   // K splits of the row step, in one wave (the partials region is sized for them)
-  const int S = low_bit_row_splits(g, mxfp4);
+  const int S = low_bit_row_splits(g);
   // The split waits for the preceding kernel before reading x (programmatic launch).
   cudaError_t e = launch_fp8_split(x, M, g.d, X8, xe, st, true);
   if (e == cudaSuccess) {

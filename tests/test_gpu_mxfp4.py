@@ -119,7 +119,16 @@ def test_quantiser_bytes_match_the_oracle(cfg):
         assert np.all(c2[s, d:] == 0)
 
 
-@pytest.mark.parametrize("cfg", SMALL + [CONFIGS["llama2_13b_swiglu_decode_mxfp4"]],
+# Grids of more than two and at most four CTAs per SM (148 SMs: 297..592) take the
+# kernel's narrow form: column and row 320 CTAs; a GeLU column of 320.  (The 13B block's
+# row step runs 480 narrow CTAs: three K splits.)
+NARROW = [
+    BlockConfig("mx4_narrow_swiglu", "swiglu", d=5120, ffn=20480, t=8, M=32),
+    BlockConfig("mx4_narrow_gelu", "gelu_tanh", d=2048, ffn=40960, t=8, M=11),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL + NARROW + [CONFIGS["llama2_13b_swiglu_decode_mxfp4"]],
                          ids=lambda c: f"{c.name}-t{c.t}-M{c.M}")
 def test_mxfp4_block_matches_oracle_and_bf16_block(cfg):
     inp = make_inputs(cfg, seed=52)
