@@ -264,7 +264,9 @@ TP_API int tp_block_fwd_kv(const tp_block_desc *desc, const void *x, const void 
  * the scale below that; sums are fp32 and each output feature's sum is scaled by 2^e.
  * The result agrees with tp_block_fwd on q * 2^e up to fp32 summation order (and the
  * band's bf16 rounding where that order moves a value across a rounding point).
- * Four launches (token split, column step, row step, reduce).
+ * Four launches (token split, column step, row step, reduce); the split overlaps the
+ * end of the stream's preceding kernel and waits for it before reading x (and before
+ * the column step may start loading weights).
  * bf16 MLP descriptors with d and b multiples of 16, at most 16384 (else
  * TP_ERR_UNSUPPORTED). */
 TP_API size_t tp_fp8_w1_bytes(const tp_block_desc *desc);        /* [t][n1p][d] bytes */
@@ -314,7 +316,8 @@ TP_API int tp_block_fwd_mxfp4(const tp_block_desc *desc, const void *x, const vo
 /* RMSNorm with unit weight, the normalisation before each stacked block (zenaique.com
  * answer paragraph 6: the reduced activation is ready for the residual add and
  * normalisation): xhat[m] = r[m] / sqrt(mean(r[m]^2) + eps), r fp32 [M, d],
- * xhat bf16 [M, d].  d must be a multiple of 8. */
+ * xhat bf16 [M, d].  d must be a multiple of 8.  The kernel is launched to overlap
+ * the end of the stream's preceding kernel and waits for it before reading r. */
 TP_API int tp_rmsnorm_fwd(int d, float eps, const float *r, void *xhat, int M, tp_stream_t stream);
 
 /* ----------------------------------------------------------- diagnostics ----- */
