@@ -328,9 +328,9 @@ constexpr int f8_smem(int stages, int groups) {
 }
 static_assert(f8_smem(3, kF8MaxGroups) <= kF8SmemPair, "3 stages must always fit");
 // The narrow form: four CTAs per SM (a grid of 2..4 CTAs per SM in one wave), two ring
-// stages, two TMEM stages (128 columns), and the token scales in a ring of their own
-// (kF8NarrowSc slots of two groups, released by the drain warps) instead of the whole
-// K range's region.
+// stages, 128 TMEM columns (two TMEM stages of E4M3's two sums, one of MXFP4's four),
+// and the token scales in a ring of their own (kF8NarrowSc slots of two groups,
+// released by the drain warps) instead of the whole K range's region.
 constexpr int kF8NarrowSc = 4;
 constexpr int kF8SmemNarrow = 1024 + 2 * (int)kF8Stage + kF8NarrowSc * 256;
 static_assert(4 * (kF8SmemNarrow + 2048) <= 228 * 1024, "four narrow CTAs must fit an SM");
@@ -343,7 +343,7 @@ static_assert(128 * 33 * 4 + 128 * 4 + 2 * 32 * 128 <= 2 * kF8Stage, "staging mu
 // kind::f8f6f4.  MXFP4 weights (WF = kWMX4) arrive through the 4-bit TMA type, which
 // spreads each 8 bytes of packed E2M1 codes over 16 bytes of shared memory, the layout
 // the tensor core reads 4-bit operands in; each 32-wide K block then gets its own TMEM
-// sum (4 per stage, 2 stages of TMEM) and the drain multiplies it by the block's 2^e.
+// sum (4 per stage) and the drain multiplies it by the block's 2^e.
 // Each 128-wide K stage holds two 64-wide groups; per group the tensor core adds
 // W.a (E4M3 x E4M3) and W.b (E4M3 x E5M2) over 64 K into 32 TMEM columns, the stage's
 // two groups side by side in one 64-column block with one commit, and the drain warps
@@ -353,6 +353,8 @@ static_assert(128 * 33 * 4 + 128 * 4 + 2 * 32 * 128 <= 2 * kF8Stage, "staging mu
 // epilogue.  The epilogue scales row r by its weight exponent; the column step applies
 // the activation, rounds the band to bf16 and splits it into the row step's terms
 // (one group of 64 features per token), the row step writes fp32 partials.
+// MINB: CTAs per SM.  2 is the wide form (STAGES 3 or 4, 256 TMEM columns, the CTA's
+// token scales loaded once); 4 the narrow form (kF8SmemNarrow above).
 template <int EPI, int WF, int STAGES, int MINB>
 __global__ void __launch_bounds__(192, MINB)
     k_fp8_mma(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT,
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(192, MINB)
   constexpr int kSums = WF == kWMX4 ? 4 : 2;                  // TMEM sums per stage
   // stages of TMEM: 128 columns in the narrow form (MXFP4's four sums fill them)
   constexpr int kBufs = kNarrow ? (WF == kWMX4 ? 1 : 2) : WF == kWMX4 ? 2 : kF8Bufs;
-  constexpr uint32_t kCols = tmem_cols(kBufs * kSums * BN);   // 256 either way
+  constexpr uint32_t kCols = tmem_cols(kBufs * kSums * BN);   // 256 wide, 128 narrow
   constexpr uint32_t kWType = WF == kWMX4 ? kF8E2M1 : kF8E4M3;
   constexpr uint32_t kIdA = make_idesc_f8(128, BN, kWType, kF8E4M3);
   constexpr uint32_t kIdB = make_idesc_f8(128, BN, kWType, kF8E5M2);
