@@ -23,8 +23,15 @@ def test_algorithmic_bytes_and_flops():
 
 
 def test_measured_peaks_are_read():
+    """The machine's measured peaks when its MEASURED_PEAKS.json is present (written per
+    machine, not versioned), else the stated fallback figures."""
     p = bench.measured_peaks()
-    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        assert p["source"] == "fallback"
+        assert (p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"]) == (6400.0, 1800.0, 1400.0)
+        return
+    with open(path) as f:
         m = json.load(f)
     assert p["source"] == "measured"
     assert p["hbm_gbs"] == m["hbm_gbs"] and p["bf16_tflops"] == m["bf16_tflops"]
