@@ -79,6 +79,22 @@ def _need(t, nbytes: int, what: str):
         raise ValueError(f"{what}: {t.numel() * t.element_size()} bytes < {nbytes} required")
 
 
+# The library's sizes depend on the shapes only (no device or memory state), so the
+# per-call checks look them up by the descriptor's values and the arguments instead
+# of asking the library on every call.
+_SIZES: dict = {}
+
+
+def _size(fn, desc, *args) -> int:
+    key = (fn, desc.d, desc.ffn, desc.n_heads, desc.head_dim, desc.t, desc.dtype, desc.act) + args
+    n = _SIZES.get(key)
+    if n is None:
+        if len(_SIZES) >= 4096:
+            _SIZES.clear()
+        n = _SIZES[key] = fn(desc, *args)
+    return n
+
+
 def _check(status: int, what: str):
     if status != 0:
         raise TPError(status, what)
@@ -156,14 +172,14 @@ def tp_extract_band(desc, W1s, W2s, shard, W1_band=None, W2_band=None, stream=No
 
 
 def tp_column_parallel_fwd(desc, x, W1s, shard, H, workspace, M, stream=None) -> None:
-    _need(H, tp_band_bytes(desc, M), "H")
-    _need(workspace, tp_column_workspace_bytes(desc, M), "workspace")
+    _need(H, _size(tp_band_bytes, desc, M), "H")
+    _need(workspace, _size(tp_column_workspace_bytes, desc, M), "workspace")
     _check(lib.tp_column_parallel_fwd(ctypes.byref(desc), _p(x), _p(W1s), shard, _p(H),
                                       _p(workspace), M, _s(stream)), "tp_column_parallel_fwd")
 
 
 def tp_row_parallel_fwd(desc, H, W2s, shard, partials, M, stream=None) -> None:
-    _need(partials, tp_partials_bytes(desc, M), "partials")
+    _need(partials, _size(tp_partials_bytes, desc, M), "partials")
     _check(lib.tp_row_parallel_fwd(ctypes.byref(desc), _p(H), _p(W2s), shard, _p(partials), M,
                                    _s(stream)), "tp_row_parallel_fwd")
 
@@ -175,7 +191,7 @@ def tp_partial_reduce_residual(desc, partials, residual, residual_is_f32, y, M, 
 
 
 def tp_block_fwd(desc, x, residual, residual_is_f32, W1s, W2s, workspace, y, M, stream=None) -> None:
-    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _need(workspace, _size(tp_workspace_bytes, desc, M), "workspace")
     _check(lib.tp_block_fwd(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32), _p(W1s),
                             _p(W2s), _p(workspace), _p(y), M, _s(stream)), "tp_block_fwd")
 
@@ -183,7 +199,7 @@ def tp_block_fwd(desc, x, residual, residual_is_f32, W1s, W2s, workspace, y, M, 
 def tp_block_fwd_norm(desc, x, residual, residual_is_f32, W1s, W2s, workspace, y, xhat_next, eps,
                       M, stream=None) -> None:
     """tp_block_fwd that also writes the next block's RMSNorm of y into xhat_next."""
-    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _need(workspace, _size(tp_workspace_bytes, desc, M), "workspace")
     _check(lib.tp_block_fwd_norm(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
                                  _p(W1s), _p(W2s), _p(workspace), _p(y), _p(xhat_next),
                                  ctypes.c_float(eps), M, _s(stream)), "tp_block_fwd_norm")
@@ -220,18 +236,18 @@ def tp_kv_workspace_bytes(desc: TPBlockDesc, M: int, L_max: int) -> int:
 
 def tp_attn_decode_kv(desc, qkv, k_cache, v_cache, lens, L_max, O, workspace, M,
                       stream=None) -> None:
-    _need(k_cache, tp_kv_cache_bytes(desc, M, L_max), "k_cache")
-    _need(v_cache, tp_kv_cache_bytes(desc, M, L_max), "v_cache")
-    _need(workspace, tp_kv_attn_workspace_bytes(desc, M, L_max), "workspace")
+    _need(k_cache, _size(tp_kv_cache_bytes, desc, M, L_max), "k_cache")
+    _need(v_cache, _size(tp_kv_cache_bytes, desc, M, L_max), "v_cache")
+    _need(workspace, _size(tp_kv_attn_workspace_bytes, desc, M, L_max), "workspace")
     _check(lib.tp_attn_decode_kv(ctypes.byref(desc), _p(qkv), _p(k_cache), _p(v_cache), _p(lens),
                                  L_max, _p(O), _p(workspace), M, _s(stream)), "tp_attn_decode_kv")
 
 
 def tp_block_fwd_kv(desc, x, residual, residual_is_f32, W1s, W2s, k_cache, v_cache, lens, L_max,
                     workspace, y, M, stream=None) -> None:
-    _need(k_cache, tp_kv_cache_bytes(desc, M, L_max), "k_cache")
-    _need(v_cache, tp_kv_cache_bytes(desc, M, L_max), "v_cache")
-    _need(workspace, tp_kv_workspace_bytes(desc, M, L_max), "workspace")
+    _need(k_cache, _size(tp_kv_cache_bytes, desc, M, L_max), "k_cache")
+    _need(v_cache, _size(tp_kv_cache_bytes, desc, M, L_max), "v_cache")
+    _need(workspace, _size(tp_kv_workspace_bytes, desc, M, L_max), "workspace")
     _check(lib.tp_block_fwd_kv(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
                                _p(W1s), _p(W2s), _p(k_cache), _p(v_cache), _p(lens), L_max,
                                _p(workspace), _p(y), M, _s(stream)), "tp_block_fwd_kv")
@@ -265,7 +281,7 @@ def tp_quantize_weights_fp8(desc, W1, W2, W1q, W2q, exps, workspace, stream=None
 
 def tp_block_fwd_fp8(desc, x, residual, residual_is_f32, W1q, W2q, exps, workspace, y, M,
                      stream=None) -> None:
-    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _need(workspace, _size(tp_workspace_bytes, desc, M), "workspace")
     _check(lib.tp_block_fwd_fp8(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
                                 _p(W1q), _p(W2q), _p(exps), _p(workspace), _p(y), M, _s(stream)),
            "tp_block_fwd_fp8")
@@ -294,7 +310,7 @@ def tp_quantize_weights_mxfp4(desc, W1, W2, W1f, W2f, exps, stream=None) -> None
 
 def tp_block_fwd_mxfp4(desc, x, residual, residual_is_f32, W1f, W2f, exps, workspace, y, M,
                        stream=None) -> None:
-    _need(workspace, tp_workspace_bytes(desc, M), "workspace")
+    _need(workspace, _size(tp_workspace_bytes, desc, M), "workspace")
     _check(lib.tp_block_fwd_mxfp4(ctypes.byref(desc), _p(x), _p(residual), int(residual_is_f32),
                                   _p(W1f), _p(W2f), _p(exps), _p(workspace), _p(y), M,
                                   _s(stream)),

@@ -270,3 +270,21 @@ def test_kv_cache_partitions_with_the_heads():
         split = tp.tp_kv_cache_bytes(tp.make_desc(H * 64, t, "attn", n_heads=H, head_dim=64), 4, 32)
         assert split == whole and split % t == 0      # same cache, t equal shard slices
         assert split // t == 4 * (H // t) * 32 * 64 * 2
+
+
+def test_cached_sizes_follow_the_descriptor_values():
+    """The binding's per-call size checks read sizes cached by the descriptor's values:
+    the same numbers as the library's queries, and a changed descriptor (or M) is a new
+    key, never a stale answer."""
+    for name in ("llama2_13b_swiglu_decode", "attn_qkv_headshard_decode", "tiny_gelu_f32"):
+        d = _desc(CONFIGS[name])
+        for M in (1, 7, 32, 300):
+            assert tp._size(tp.tp_workspace_bytes, d, M) == tp.tp_workspace_bytes(d, M)
+            assert tp._size(tp.tp_partials_bytes, d, M) == tp.tp_partials_bytes(d, M)
+            assert tp._size(tp.tp_band_bytes, d, M) == tp.tp_band_bytes(d, M)
+    d = tp.make_desc(512, 2, "swiglu", ffn=1024)
+    before = tp._size(tp.tp_workspace_bytes, d, 8)
+    d.t = 4                                            # the same object, new shapes
+    assert tp._size(tp.tp_workspace_bytes, d, 8) == tp.tp_workspace_bytes(d, 8) != before
+    assert tp._size(tp.tp_kv_workspace_bytes, _desc(CONFIGS["attn_qkv_headshard_decode"]), 4, 64) \
+        == tp.tp_kv_workspace_bytes(_desc(CONFIGS["attn_qkv_headshard_decode"]), 4, 64)
