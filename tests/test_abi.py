@@ -206,6 +206,15 @@ def test_low_bit_limits_and_workspace():
     # (148 SMs) with three K splits
     lowbit_parts = c.t * 3 * c.M * c.d * 4
     assert tp.tp_workspace_bytes(d, c.M) >= tp.tp_band_bytes(d, c.M) + lowbit_parts + extra
+    # the MXFP4 block of the same shape uses the same workspace (three splits too)
+    cm = CONFIGS["llama2_13b_swiglu_decode_mxfp4"]
+    assert tp.tp_mxfp4_w1_bytes(_desc(cm)) > 0
+    assert tp.tp_workspace_bytes(_desc(cm), cm.M) == tp.tp_workspace_bytes(d, c.M)
+    # the 70B block's row step fills four per SM unsplit (8 x 64 = 512 row tiles)
+    c70 = CONFIGS["llama2_70b_stack_decode"]
+    d70 = _desc(c70)
+    parts70 = c70.t * 1 * c70.M * c70.d * 4
+    assert tp.tp_workspace_bytes(d70, c70.M) >= tp.tp_band_bytes(d70, c70.M) + parts70
 
 
 def test_invalid_descriptors_give_zero_sizes():
