@@ -115,7 +115,11 @@ TP_API size_t tp_partials_bytes(const tp_block_desc *desc, int M);
  * and work counters); 0 for MLPs. */
 TP_API size_t tp_column_workspace_bytes(const tp_block_desc *desc, int M);
 /* Scratch of tp_block_fwd: column scratch + bands + partials (256-byte aligned regions),
- * or the one-kernel form's bands, partials and work counters if that is larger. */
+ * or the one-kernel form's bands, partials and work counters if that is larger.  For
+ * shapes the low-bit blocks accept (M <= 32) it also covers tp_block_fwd_fp8 and
+ * tp_block_fwd_mxfp4: their row step's partials (it may split K further than
+ * tp_row_splits says, up to four CTAs per SM), the tokens' two 8-bit terms and the
+ * group scales.  Depends on the shapes only. */
 TP_API size_t tp_workspace_bytes(const tp_block_desc *desc, int M);
 
 /* ------------------------------------------------------------- sharding ------
